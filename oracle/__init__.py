@@ -1,0 +1,30 @@
+"""CPU oracle for SageAttention-style quantized attention — TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, obviously-correct restatement of what the GPU path
+computes, written from the method's description (pwwt.cn "SageAttention deployment
+pitfalls guide", §1 "why attention is the bottleneck" for the three-stage idea, §4.1/§4.2
+for the API knobs qk_quant_gran / pv_accum_dtype / smooth_k / smooth_v, §4 for
+sageattn_varlen) plus the readings listed in the design doc where the pages are silent.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl
+reference`` legs of ``bench.py`` may import it. The product path
+(``quantized_attention_mean_gb300``) never does: it shares no code, table or helper with
+this package, and fails loudly when its CUDA library is missing.
+
+All floating-point work that is not explicitly a quantisation step runs in float64.
+The quantisation steps run in float32 exactly as the method's scale/reciprocal/round
+sequence defines them, so that integer and FP8 codes can be compared bit for bit.
+
+Parity status per function (see the pins in ``tests/test_oracle_*.py``):
+  fp8.e4m3_encode / e4m3_decode          pinned (brute-force nearest-value search, spec table)
+  quant.fixed_point_mean                 pinned (exact rational arithmetic)
+  quant.int8_group_quant                 pinned (hand-derived cases, round-trip bound, extremes)
+  quant.fp8_channel_quant                pinned (bound + extremes + brute force)
+  attention.sage_attention               pinned (closed forms: Nk=1, uniform keys, constant V,
+                                          causal row 0; quantisation bypass == fp64 attention;
+                                          smooth_k invariance; cosine vs fp64)
+  attention fp16+fp32 accumulation       parity unpinned beyond the bypass/closed forms: the
+                                          in-tile rounding order is a reading, not a definition
+"""
+
+from . import fp8, quant, attention  # noqa: F401

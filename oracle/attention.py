@@ -1,0 +1,252 @@
+"""Stage 3 of the method and the whole forward pass (test oracle).
+
+pwwt.cn "SageAttention deployment pitfalls guide":
+  §1   the product QK^T runs on 8-bit integers, P·V on FP8 with FP16/FP32 accumulators,
+       the output stays FP16/BF16;
+  §4.1 sageattn(q, k, v, tensor_layout, is_causal, sm_scale=None -> 1/sqrt(head_dim),
+       return_lse); head_dim padding rule; GQA (Hq divisible by Hkv); Nq may differ
+       from Nk;
+  §4.2 pv_accum_dtype in {fp16, fp32, fp16+fp32};
+  §4 (end) sageattn_varlen with cu_seqlens_q / cu_seqlens_k.
+
+The steps, in the order the method applies them, per (batch, query head):
+  1. k̄, v̄ = fixed-point means over the sequence (smooth_k / smooth_v; 0 when off)
+  2. K' = K - k̄, V' = V - v̄ (float32)
+  3. Q, K' -> INT8 per token group; V' -> E4M3 per channel
+  4. S = Q8 · K8^T, exact integers
+  5. t = S · s_q · s_k · sm_scale, causal mask (key j allowed iff j <= i), in float64
+  6. m = row max of t (final max), p = exp(t - m), l = sum p
+  7. P~ = e4m3(p · σ_P), σ_P = 448 (fp32 accumulation) or 1 (fp16+fp32)
+  8. acc = P~ · V~ (fp32 modes: float64 sum; fp16+fp32: each 128-key tile's partial
+     rounded to fp16 before the float64 sum)
+  9. O = acc · s_v / (σ_P · l) + v̄, rounded once to the output dtype
+ 10. LSE = m + ln l + sm_scale · (q · k̄)   (natural log; undoes the smooth_k shift)
+Steps 5-10 use library matmuls on exact integer or float64 operands only.
+"""
+
+import numpy as np
+
+from .fp8 import e4m3_decode, e4m3_encode
+from .quant import (GRAN_PER_BLOCK, GRAN_PER_THREAD, GRAN_PER_WARP, K_GROUP, Q_GROUP,
+                    fixed_point_mean, fp8_channel_quant, int8_group_quant, smooth)
+
+ACC_FP32, ACC_FP16_FP32, ACC_FP32_FP32, ACC_FP16 = 0, 1, 2, 3
+PV_TILE = 128  # keys per P·V tile for the fp16+fp32 in-tile rounding
+
+__all__ = [
+    "ACC_FP32", "ACC_FP16_FP32", "ACC_FP32_FP32", "ACC_FP16", "GRAN_PER_BLOCK",
+    "GRAN_PER_WARP", "GRAN_PER_THREAD", "default_sm_scale", "quantize_kv_head",
+    "quantize_q_head", "scores", "attend_head", "sage_attention", "sage_attention_varlen",
+    "attention_fp64", "round_float", "to_fp16", "to_bf16",
+]
+
+
+def default_sm_scale(head_dim):
+    """§4.1: sm_scale=None means 1/sqrt(head_dim) of the caller's (unpadded) head_dim."""
+    return float(np.float32(1.0 / np.sqrt(np.float64(head_dim))))
+
+
+def sigma_p(accum):
+    if accum == ACC_FP16:
+        raise NotImplementedError("pure fp16 P·V accumulation is not supported")
+    return 1.0 if accum == ACC_FP16_FP32 else 448.0
+
+
+def round_float(x, sig_bits, min_normal_exp, max_finite):
+    """Round float64 values to a binary format with `sig_bits` significand bits, RNE."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex.astype(np.int64) - 1, min_normal_exp)
+    qexp = e - (sig_bits - 1)
+    r = np.ldexp(np.rint(np.ldexp(a, -qexp)), qexp)
+    r = np.where(r > max_finite, np.inf, r)
+    return np.copysign(r, x)
+
+
+def to_fp16(x):
+    return round_float(x, 11, -14, 65504.0)
+
+
+def to_bf16(x):
+    return round_float(x, 8, -126, float.fromhex("0x1.fep127"))
+
+
+# --------------------------------------------------------------------------- stages 1-3
+def quantize_kv_head(k, v, gran, smooth_k, smooth_v):
+    """Stages 1-3 for one KV head: k, v float32 [Nk, d]."""
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    d = k.shape[1]
+    kbar = fixed_point_mean(k) if smooth_k else np.zeros(d, np.float32)
+    vbar = fixed_point_mean(v) if smooth_v else np.zeros(d, np.float32)
+    ks = smooth(k, kbar)
+    vs = smooth(v, vbar)
+    k8, sk = int8_group_quant(ks, K_GROUP[gran])
+    v8, sv = fp8_channel_quant(vs)
+    return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk, v8=v8, sv=sv)
+
+
+def quantize_q_head(q, gran):
+    q8, sq = int8_group_quant(np.asarray(q, np.float32), Q_GROUP[gran])
+    return dict(q8=q8, sq=sq)
+
+
+# --------------------------------------------------------------------------- steps 4-10
+def scores(q8, k8):
+    """Step 4 alone: S = Q8 · K8^T as exact int64 (the INT32 score contract)."""
+    return np.asarray(q8, np.int64) @ np.asarray(k8, np.int64).T
+
+
+def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
+                bypass_quant=False, row_chunk=512):
+    """Steps 4-10 for one query head against one quantised KV head.
+
+    q: float32 [Nq, d] (original values, used for Q quantisation and the LSE term);
+    kvq: output of quantize_kv_head; rows: query rows to compute (default all).
+    bypass_quant replaces every code by the value it encodes (scales 1, P unrounded):
+    the result must then equal exact attention, which pins the non-quantising steps.
+    Returns dict(o=float64 [R, d] before output rounding, lse=float64 [R]).
+    """
+    q = np.asarray(q, np.float32)
+    nq, d = q.shape
+    nk = kvq["k8"].shape[0]
+    rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    sig = sigma_p(accum)
+    if bypass_quant:
+        qv = q.astype(np.float64)
+        sq_row = np.ones(nq)
+        kv = kvq["k_smoothed"].astype(np.float64)
+        sk_key = np.ones(nk)
+        vd = kvq["v_smoothed"].astype(np.float64)
+        sv = np.ones(d)
+    else:
+        if qq is None:
+            qq = quantize_q_head(q, gran)
+        qv = qq["q8"].astype(np.float64)
+        sq_row = qq["sq"].astype(np.float64)[np.arange(nq) // Q_GROUP[gran]]
+        kv = kvq["k8"].astype(np.float64)
+        sk_key = kvq["sk"].astype(np.float64)[np.arange(nk) // K_GROUP[gran]]
+        vd = e4m3_decode(kvq["v8"])
+        sv = kvq["sv"].astype(np.float64)
+    vbar = kvq["vbar"].astype(np.float64)
+    kbar = kvq["kbar"].astype(np.float64)
+
+    o = np.empty((len(rows), d))
+    lse = np.empty(len(rows))
+    keys = np.arange(nk)
+    for c0 in range(0, len(rows), row_chunk):
+        r = rows[c0:c0 + row_chunk]
+        s = qv[r] @ kv.T                                   # step 4 (exact for integer codes)
+        t = s * (sq_row[r][:, None] * sk_key[None, :] * sm_scale)  # step 5
+        if is_causal:
+            t = np.where(keys[None, :] <= r[:, None], t, -np.inf)
+        m = t.max(axis=1)                                  # step 6
+        p = np.exp(t - m[:, None])
+        l = p.sum(axis=1)
+        if bypass_quant:                                   # step 7
+            pq = p * sig
+        else:
+            pq = e4m3_decode(e4m3_encode(p * sig))
+        if accum == ACC_FP16_FP32 and not bypass_quant:   # step 8
+            acc = np.zeros((len(r), d))
+            for k0 in range(0, nk, PV_TILE):
+                acc += to_fp16(pq[:, k0:k0 + PV_TILE] @ vd[k0:k0 + PV_TILE])
+        else:
+            acc = pq @ vd
+        o[c0:c0 + len(r)] = acc * sv[None, :] / (sig * l[:, None]) + vbar[None, :]  # step 9
+        lse[c0:c0 + len(r)] = m + np.log(l) + sm_scale * (q[r].astype(np.float64) @ kbar)  # 10
+    return dict(o=o, lse=lse)
+
+
+def _check_args(hq, hkv, d, accum):
+    if d < 1 or d > 128:
+        raise ValueError("head_dim must be in [1, 128]")
+    if hkv < 1 or hq % hkv:
+        raise ValueError("query heads must be a multiple of KV heads")
+    sigma_p(accum)
+
+
+def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WARP,
+                   accum=ACC_FP32, smooth_k=True, smooth_v=False, heads=None, rows=None,
+                   bypass_quant=False):
+    """Dense forward on canonical float32 arrays q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d].
+
+    heads: optional list of (b, hq) pairs to compute (default all); rows: optional query
+    rows (same for every computed head). Returns dict with o [B, Hq, R, d] and lse
+    [B, Hq, R] (NaN for heads not computed) and the per-head quantised tensors.
+    """
+    q = np.asarray(q, np.float32)
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    b_, hq, nq, d = q.shape
+    hkv, nk = k.shape[1], k.shape[2]
+    _check_args(hq, hkv, d, accum)
+    if nk == 0:
+        raise ValueError("attention over zero keys is undefined")
+    if sm_scale is None:
+        sm_scale = default_sm_scale(d)
+    group = hq // hkv
+    heads = [(b, h) for b in range(b_) for h in range(hq)] if heads is None else heads
+    nr = nq if rows is None else len(rows)
+    o = np.full((b_, hq, nr, d), np.nan)
+    lse = np.full((b_, hq, nr), np.nan)
+    kvcache, qcache = {}, {}
+    for (b, h) in heads:
+        key = (b, h // group)
+        if key not in kvcache:
+            kvcache[key] = quantize_kv_head(k[b, h // group], v[b, h // group], gran,
+                                            smooth_k, smooth_v)
+        qcache[(b, h)] = quantize_q_head(q[b, h], gran)
+        res = attend_head(q[b, h], kvcache[key], gran=gran, sm_scale=sm_scale,
+                          is_causal=is_causal, accum=accum, rows=rows, qq=qcache[(b, h)],
+                          bypass_quant=bypass_quant)
+        o[b, h] = res["o"]
+        lse[b, h] = res["lse"]
+    return dict(o=o, lse=lse, kv=kvcache, q=qcache, sm_scale=sm_scale)
+
+
+def sage_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, **kw):
+    """Variable-length forward on packed float32 q [Tq, Hq, d], k/v [Tk, Hkv, d].
+
+    Sequence b spans tokens [cu[b], cu[b+1]); smoothing means, quantisation groups and
+    the causal mask all restart per sequence. Returns o [Tq, Hq, d] and lse [Hq, Tq].
+    """
+    q = np.asarray(q, np.float32)
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    cq = np.asarray(cu_seqlens_q, np.int64)
+    ck = np.asarray(cu_seqlens_k, np.int64)
+    tq, hq, d = q.shape
+    o = np.full((tq, hq, d), np.nan)
+    lse = np.full((hq, tq), np.nan)
+    per_seq = []
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            per_seq.append(None)
+            continue
+        qs = q[q0:q1].transpose(1, 0, 2)[None]
+        ks = k[k0:k1].transpose(1, 0, 2)[None]
+        vs = v[k0:k1].transpose(1, 0, 2)[None]
+        res = sage_attention(qs, ks, vs, **kw)
+        o[q0:q1] = res["o"][0].transpose(1, 0, 2)
+        lse[:, q0:q1] = res["lse"][0]
+        per_seq.append(res)
+    return dict(o=o, lse=lse, per_seq=per_seq)
+
+
+# --------------------------------------------------------------------------- fp64 reference
+def attention_fp64(q, k, v, sm_scale, is_causal, rows=None):
+    """Exact softmax(q k^T · sm_scale) v for one head, float64. Returns (o, lse)."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows, np.int64)
+    t = (q[rows] @ k.T) * sm_scale
+    if is_causal:
+        t = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], t, -np.inf)
+    m = t.max(axis=1)
+    p = np.exp(t - m[:, None])
+    l = p.sum(axis=1)
+    return (p @ v) / l[:, None], m + np.log(l)

@@ -1,0 +1,360 @@
+"""Benchmark: quantized attention TOPS (4·B·H·Nq·Nk·d / s, halved for causal) on GB300.
+
+One step = one full sage_attn call (K/V statistics + quantisation + fused attention) on one
+batch of synthetic inputs of the 4K self-attention workload (B=2, H=8, Nq=Nk=4096, d=128,
+fp16, HND, non-causal, per_warp INT8 Q/K, smooth_k, FP8 V, fp16+fp32 P.V accumulation).
+Inputs rotate over several resident sets whose footprint exceeds the 129 MB L2, so no step
+starts with its inputs cached.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
+
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no collective on the
+data path); rank 0 prints one JSON line with the max time over ranks.
+`--impl reference` times the CPU oracle (the slow, plain restatement of the method) on a
+bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized attention TOPS (4·B·H·Nq·Nk·d/s) at 1 GB300; % of INT8/FP8 tensor peak"
+UNIT = "TOPS"
+L2_BYTES = 129 * 2**20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sdpa4k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def describe(w):
+    lay = f"{w.B}x{w.Hq}" + (f"/{w.Hkv}" if w.Hkv != w.Hq else "")
+    return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq={w.Nq} Nk={w.Nk} d={w.d} {w.dtype} "
+            f"{w.layout} causal={int(w.is_causal)} {w.gran} smooth_k={int(w.smooth_k)} "
+            f"smooth_v={int(w.smooth_v)} pv_accum={w.accum} lse={int(w.return_lse)} ({lay})")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sust=m["bf16_tflops_sustained"],
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, local, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(ws, dev=None):
+    if ws > 1:
+        import torch.distributed as dist
+        if dev is not None:
+            dist.barrier(device_ids=[dev.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x, ws, dev=None):
+    """Max of a float over ranks (identity for one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev if dev is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(ops_per_rank_step, steps, max_seconds, ws):
+    """Whole-job throughput: all ranks' units over the slowest rank's time (weak scaling)."""
+    return ops_per_rank_step * steps * ws / max_seconds / 1e12
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, rows, seed=0):
+    """Times the oracle on one (batch 0, head 0) slice: that head's K/V and Q quantisation and
+    `rows` query rows of attention. Returns (ops, seconds)."""
+    import numpy as np
+    from oracle.attention import attend_head, quantize_kv_head, quantize_q_head, default_sm_scale
+    from quantized_attention_mean_gb300.workloads import ACC, GRAN, dense_inputs, to_hnd_f32
+    q, k, v = dense_inputs(w, seed)
+    qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
+    g = GRAN[w.gran]
+    t0 = time.perf_counter()
+    kvq = quantize_kv_head(kn[0, 0], vn[0, 0], g, w.smooth_k, w.smooth_v)
+    qq = quantize_q_head(qn[0, 0], g)
+    attend_head(qn[0, 0], kvq, gran=g, sm_scale=default_sm_scale(w.d), is_causal=w.is_causal,
+                accum=ACC[w.accum], rows=np.arange(rows), qq=qq)
+    dt = time.perf_counter() - t0
+    ops = 4.0 * rows * w.Nk * w.d / (2.0 if w.is_causal else 1.0)
+    return ops, dt
+
+
+def cpu_baseline_subprocess(wname, rows):
+    """Runs the oracle sample in a fresh single-threaded process (BLAS pinned to 1 thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench, json; "
+            f"from quantized_attention_mean_gb300.workloads import WORKLOADS; "
+            f"print(json.dumps(bench.oracle_sample(WORKLOADS[{wname!r}], {rows})))")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    ops, dt = json.loads(r.stdout.strip().splitlines()[-1])
+    return ops, dt
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    rows = 256
+    for _ in range(args.warmup):
+        oracle_sample(w, rows)
+    tot_ops, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        ops, dt = oracle_sample(w, rows)
+        tot_ops += ops
+        tot_s += dt
+    value = tot_ops / tot_s / 1e12
+    cores = os.cpu_count()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": describe(w), "parallelism": "none (host CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: batch 0 head 0 of {w.name}: K/V/Q quantisation of the head "
+                                   f"+ {rows} of {w.Nq} query rows; numpy (BLAS may thread)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import quantized_attention_mean_gb300 as qa
+    from quantized_attention_mean_gb300.workloads import dense_inputs
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws_n, local, "nccl")
+    pk = peaks()
+
+    # resident input sets: enough that one pass over them exceeds L2
+    q0, k0, v0 = dense_inputs(w, seed=rank)
+    per_set = sum(t.numel() * t.element_size() for t in (q0, k0, v0)) * 4 // 3  # + output
+    wsb = qa.workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran)
+    nsets = max(2, -(-2 * L2_BYTES // (per_set + wsb)))
+    sets = []
+    for i in range(nsets):
+        q, k, v = (t.to(dev) for t in dense_inputs(w, seed=rank * 100 + i))
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev) if w.return_lse else None
+        ws = qa.alloc_workspace(wsb, dev)
+        sets.append((q, k, v, out, lse, ws))
+    kw = dict(tensor_layout=w.layout, is_causal=w.is_causal, return_lse=w.return_lse,
+              qk_quant_gran=w.gran, pv_accum_dtype=w.accum, smooth_k=w.smooth_k, smooth_v=w.smooth_v)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        q, k, v, out, lse, ws = sets[i % nsets]
+        qa.sage_attn(q, k, v, out=out, lse=lse, workspace=ws, **kw)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    assert qa.read_device_status(sets[0][5]) == 0
+
+    ops = w.ops()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    qa.profile_enable(True)
+    barrier(ws_n, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n, dev)
+    elapsed_ms = e0.elapsed_time(e1)
+    stage_ms, calls = qa.profile_read()
+    qa.profile_enable(False)
+    clocks = sampler.stop()
+    for s in sets:
+        assert qa.read_device_status(s[5]) == 0
+    max_s = max_over_ranks(elapsed_ms / 1e3, ws_n, dev)
+    value = aggregate(ops, args.steps, max_s, ws_n)
+
+    # roofline of the dominant kernel (the fused attention kernel): algorithmic ops per launch
+    # over its mean event-timed duration; peak = dense FP8 = measured bf16 burst x 2
+    attn_ms = stage_ms[2] / max(calls, 1)
+    achieved = ops / (attn_ms / 1e3) / 1e12
+    fp8_peak = 2.0 * pk["bf16"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": None,
+                "kernel": "attn_kernel<128> (fused QK^T/softmax/PV)",
+                "peak_source": f"{pk['src']}: dense FP8 = 2 x bf16 burst {pk['bf16']} TFLOP/s",
+                "route_ceiling_frac": 2.0 / 3.0,
+                "stage_ms_per_step": {"stats": stage_ms[0] / max(calls, 1),
+                                      "quant": stage_ms[1] / max(calls, 1), "attention": attn_ms}}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in dense_inputs(w, seed=rank))
+        ho = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev)
+        dout = torch.empty_like(dq)
+        wse = qa.alloc_workspace(wsb, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size()
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            qa.sage_attn(dq, dk, dv, out=dout, workspace=wse, **{**kw, "return_lse": False})
+            ho.copy_(dout, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 100))
+        barrier(ws_n, dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n, dev)
+        e2e_s = max_over_ranks(f0.elapsed_time(f1) / 1e3, ws_n, dev)
+        e2e = {"value": aggregate(ops, n_e2e, e2e_s, ws_n), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        rows = 512
+        c_ops, c_s = cpu_baseline_subprocess(w.name, rows)
+        cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"batch 0 head 0 of {w.name}: that head's K/V/Q quantisation + {rows} of "
+                         f"{w.Nq} query rows ({c_ops:.3g} ops in {c_s:.1f} s, 1 thread)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 QK (exact, fp16 carrier) + e4m3 PV, fp32 softmax",
+            "data": "synthetic",
+            "config": {"workload": describe(w), "parallelism": f"replicas x{ws_n} (independent heads/batches)",
+                       "l2": f"inputs rotate over {nsets} resident sets ({nsets * (per_set + wsb) / 2**20:.0f} MiB > L2 129 MiB)"},
+            "pct_fp8_peak": value / fp8_peak,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from quantized_attention_mean_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if w.varlen:
+        raise SystemExit("bench: varlen workloads are measured by tests, not this entry point")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * sageattn.h — C ABI of libsageattn.so: SageAttention-style quantized attention forward,
+ * O = softmax(Q K^T · sm_scale) V, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (pwwt.cn "SageAttention deployment pitfalls guide"):
+ *   §1   Q and K are quantized to INT8 with fine-grained scales and QK^T runs on the
+ *        8-bit values; V is quantized to FP8 and P·V runs with FP16/FP32 accumulators;
+ *        the output stays FP16/BF16.
+ *   §4.1 sageattn(q, k, v, tensor_layout="HND"|"NHD", is_causal, sm_scale=None,
+ *        return_lse): inputs FP16 or BF16 on one device with one dtype, last dimension
+ *        contiguous; head_dim below 64 is zero-padded to 64, between 64 and 128 to 128,
+ *        above 128 is an error; Hq must be a multiple of Hkv (GQA); Nq may differ from Nk.
+ *   §4.2 qk_quant_gran (per_warp / per_thread; per_block added), pv_accum_dtype
+ *        (fp16 / fp32 / fp16+fp32), smooth_k (subtract K's mean over the sequence),
+ *        smooth_v (same for V).
+ *   §4 (end) sageattn_varlen: variable-length batches given by cu_seqlens_q / cu_seqlens_k.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device pointers on the current device; the caller
+ *     owns every buffer (inputs, outputs, LSE, workspace). The library never allocates or
+ *     frees device memory, never synchronises inside sage_attn / sage_attn_varlen, and
+ *     enqueues all work on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Arguments are validated on the host before anything is launched: on a non-zero
+ *     return nothing was written. Errors found on the device (a bad cu_seqlens, a value
+ *     too large for the exact mean, a pipeline wait that timed out) are recorded in the
+ *     workspace and read back with sage_read_device_status().
+ *   - Strides are in elements. The channel (head_dim) stride is always 1.
+ *   - The workspace must be 256-byte aligned, at least sage_attn_workspace_size() bytes,
+ *     and must not be shared by calls that may run concurrently.
+ *   - Thread safety: calls from several host threads are safe; the only global state is a
+ *     per-device cache of the kernels' shared-memory opt-in.
+ */
+#ifndef SAGEATTN_H
+#define SAGEATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, Nk == 0 with Nq > 0 */
+  SAGE_ERR_HEAD_DIM = 2,     /* head_dim < 1 or > 128 */
+  SAGE_ERR_DTYPE = 3,        /* dtype not SAGE_F16 / SAGE_BF16 */
+  SAGE_ERR_STRIDE = 4,       /* misaligned pointer or a stride that breaks the layout rules */
+  SAGE_ERR_GQA = 5,          /* Hq not a multiple of Hkv */
+  SAGE_ERR_WORKSPACE = 6,    /* workspace null, misaligned or too small */
+  SAGE_ERR_RANGE = 7,        /* (device) |x| >= 2^38 / N: too large for the exact mean */
+  SAGE_ERR_UNSUPPORTED = 8,  /* pv_accum_dtype SAGE_ACC_FP16 */
+  SAGE_ERR_TIMEOUT = 9,      /* (device) a bounded pipeline wait expired */
+  SAGE_ERR_CUDA = 10,        /* a CUDA runtime/driver call failed */
+  SAGE_ERR_DEVICE = 11,      /* current device is not compute capability 10.3 */
+  SAGE_ERR_SEQLENS = 12      /* (device) cu_seqlens not non-decreasing / out of range */
+} sage_status;
+
+enum { SAGE_HND = 0, SAGE_NHD = 1 };                       /* §4.1 tensor_layout */
+enum { SAGE_F16 = 0, SAGE_BF16 = 1 };                      /* input/output dtype */
+enum { SAGE_PER_BLOCK = 0, SAGE_PER_WARP = 1, SAGE_PER_THREAD = 2 };   /* qk_quant_gran */
+enum { SAGE_ACC_FP32 = 0, SAGE_ACC_FP16_FP32 = 1, SAGE_ACC_FP32_FP32 = 2, SAGE_ACC_FP16 = 3 };
+
+/* A 4-d FP16/BF16 device tensor in the order the call's tensor_layout names:
+ * HND = [batch, heads, seq, head_dim], NHD = [batch, seq, heads, head_dim].
+ * stride[0..2] are the element strides of the first three dimensions; the fourth
+ * (channel) stride is 1. `data` points at element [0, 0, 0, 0]. */
+typedef struct {
+  void* data;
+  int64_t stride[3];
+} sage_tensor;
+
+/* A packed variable-length FP16/BF16 device tensor [total_tokens, heads, head_dim]
+ * with element strides per token and per head; the channel stride is 1. */
+typedef struct {
+  void* data;
+  int64_t stride_token;
+  int64_t stride_head;
+} sage_packed;
+
+/* Bytes of workspace sage_attn needs for these sizes (0 on invalid sizes). */
+size_t sage_attn_workspace_size(int batch, int heads_q, int heads_kv, int seqlen_q,
+                                int seqlen_k, int head_dim, int qk_quant_gran);
+
+/* Dense forward (§4.1, §4.2).
+ *   q [B, Hq, Nq, d] / [B, Nq, Hq, d]; k, v [B, Hkv, Nk, d] / [B, Nk, Hkv, d] (device,
+ *   read only); out: same shape and layout as q (device, written, dtype = input dtype).
+ *   lse: device float [B, Hq, Nq] contiguous, natural-log log-sum-exp of the scaled
+ *   scores sm_scale·q·k over the allowed keys; written only when return_lse != 0
+ *   (may be NULL otherwise).
+ *   is_causal: key j is allowed for query i iff j <= i (top-left aligned, as
+ *   torch.nn.functional.scaled_dot_product_attention).
+ *   sm_scale: scale of the scores; NaN or <= 0 selects 1/sqrt(head_dim).
+ *   qk_quant_gran: token groups sharing one INT8 scale — per_block 128 Q rows / 64 K rows,
+ *   per_warp 32 / 64, per_thread 1 / 16.
+ *   pv_accum_dtype: SAGE_ACC_FP32 or SAGE_ACC_FP32_FP32 (P scaled by 448 before FP8,
+ *   fp32 accumulation), SAGE_ACC_FP16_FP32 (P unscaled, each 128-key partial rounded to
+ *   fp16 and summed in fp32); SAGE_ACC_FP16 returns SAGE_ERR_UNSUPPORTED.
+ *   smooth_k / smooth_v: subtract the per-(batch, head, channel) mean over the sequence.
+ *   Nq == 0 or B == 0 is a no-op returning SAGE_OK.
+ * Returns a sage_status. */
+int sage_attn(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+              const sage_tensor* out, float* lse, int batch, int heads_q, int heads_kv,
+              int seqlen_q, int seqlen_k, int head_dim, int dtype, int tensor_layout,
+              int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+              int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace sage_attn_varlen needs (0 on invalid sizes). */
+size_t sage_attn_varlen_workspace_size(int batch, int heads_q, int heads_kv, int total_q,
+                                       int total_k, int head_dim, int qk_quant_gran);
+
+/* Variable-length forward (§4, sageattn_varlen). Sequence b owns query tokens
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q and key tokens [cu_seqlens_k[b],
+ * cu_seqlens_k[b+1]) of k and v; smoothing means, quantisation groups and the causal mask
+ * restart per sequence.
+ *   q, out: [total_q, Hq, d]; k, v: [total_k, Hkv, d] (device).
+ *   cu_seqlens_q, cu_seqlens_k: device int32 [batch + 1], non-decreasing, starting at 0
+ *   and ending at total_q / total_k (checked on the device: SAGE_ERR_SEQLENS).
+ *   max_seqlen_q / max_seqlen_k: upper bounds of the lengths (checked on the device).
+ *   lse: device float [Hq, total_q] when return_lse != 0.
+ *   A sequence with no keys but some queries is a device error (SAGE_ERR_SEQLENS).
+ * Other arguments as sage_attn. */
+int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_packed* v,
+                     const sage_packed* out, float* lse, const int32_t* cu_seqlens_q,
+                     const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
+                     int max_seqlen_k, int total_q, int total_k, int heads_q, int heads_kv,
+                     int head_dim, int dtype, int is_causal, float sm_scale, int return_lse,
+                     int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a sage_status. Never NULL. */
+const char* sage_status_string(int status);
+
+/* Synchronises `stream`, then returns the status the device recorded in `workspace`
+ * during the last call that used it (SAGE_OK if none), or SAGE_ERR_CUDA. */
+int sage_read_device_status(const void* workspace, void* stream);
+
+/* 1 if the current CUDA device is compute capability 10.3 (GB300), else 0. */
+int sage_device_supported(void);
+
+/* Stage timing (off by default). While enabled, every sage_attn / sage_attn_varlen call
+ * records CUDA events on its stream around its three stages (statistics, quantisation,
+ * attention kernel); up to 8192 calls are kept. sage_profile_read synchronises those events
+ * and writes the summed milliseconds per stage to stage_ms[0..2] and the number of calls to
+ * *calls; it also clears the record. Enabling allocates CUDA events (no device memory).
+ * Returns a sage_status. */
+int sage_profile_enable(int on);
+int sage_profile_read(double* stage_ms, int* calls);
+
+/* ---- Test exports. They run the same kernels as the entry points above. ---- */
+
+/* Copies the quantised state that the last sage_attn call with these sizes left in
+ * `workspace` into canonical host-layout device buffers (all device, caller-owned):
+ *   q8 int8 [B, Hq, Nq, d], sq float [B, Hq, ceil(Nq / Gq)],
+ *   k8 int8 [B, Hkv, Nk, d], sk float [B, Hkv, ceil(Nk / Gk)],
+ *   kmean, vmean, vscale float [B, Hkv, d], v8 uint8 E4M3 [B, Hkv, Nk, d].
+ * Any output pointer may be NULL to skip it. */
+int sage_debug_export_quant(const void* workspace, int batch, int heads_q, int heads_kv,
+                            int seqlen_q, int seqlen_k, int head_dim, int qk_quant_gran,
+                            int8_t* q8, float* sq, int8_t* k8, float* sk, float* kmean,
+                            float* vmean, float* vscale, uint8_t* v8, void* stream);
+
+/* sage_attn that additionally writes the integer scores S = Q8 · K8^T, exactly as the
+ * attention kernel reads them from tensor memory, to `scores` (device int32
+ * [B, Hq, Nq, Nk]; entries the causal mask skips are left untouched). */
+int sage_attn_debug_scores(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                           const sage_tensor* out, float* lse, int batch, int heads_q,
+                           int heads_kv, int seqlen_q, int seqlen_k, int head_dim, int dtype,
+                           int tensor_layout, int is_causal, float sm_scale, int return_lse,
+                           int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
+                           void* workspace, size_t workspace_bytes, int32_t* scores,
+                           void* stream);
+
+/* Converts n floats (device) to FP8 E4M3 (device bytes) with the round-to-nearest-even,
+ * saturating conversion the kernels use for V and P. */
+int sage_debug_e4m3(const float* x, uint8_t* out, int64_t n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGEATTN_H */

@@ -1,0 +1,207 @@
+"""SageAttention-style quantized attention forward for one GB300 (sm_103a).
+
+Thin Python binding over libsageattn.so (include/sageattn.h). PyTorch only supplies device
+memory and streams; every step of the computation runs in the library's CUDA kernels.
+
+    out = sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None,
+                    return_lse=False, qk_quant_gran="per_warp", pv_accum_dtype="fp32",
+                    smooth_k=True, smooth_v=False)
+
+mirrors the ``sageattn`` API (pwwt.cn "SageAttention deployment pitfalls guide" §4.1, §4.2);
+``sage_attn_varlen`` mirrors ``sageattn_varlen``.
+"""
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import SagePacked, SageTensor
+
+GRAN = {"per_block": 0, "per_warp": 1, "per_thread": 2}
+ACC = {"fp32": 0, "fp16+fp32": 1, "fp32+fp32": 2, "fp16": 3}
+LAYOUT = {"HND": 0, "NHD": 1}
+DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+class SageError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        msg = _lib.load().sage_status_string(status).decode()
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def _check(status, what):
+    if status != 0:
+        raise SageError(status, what)
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _tensor(t):
+    st = t.stride()
+    if st[3] != 1:
+        raise ValueError("the last dimension must be contiguous")
+    return SageTensor(t.data_ptr(), (ctypes.c_int64 * 3)(st[0], st[1], st[2]))
+
+
+def _packed(t):
+    st = t.stride()
+    if st[2] != 1:
+        raise ValueError("the last dimension must be contiguous")
+    return SagePacked(t.data_ptr(), st[0], st[1])
+
+
+def workspace_bytes(batch, heads_q, heads_kv, seqlen_q, seqlen_k, head_dim, qk_quant_gran="per_warp"):
+    return _lib.load().sage_attn_workspace_size(batch, heads_q, heads_kv, seqlen_q, seqlen_k,
+                                                head_dim, GRAN[qk_quant_gran])
+
+
+def varlen_workspace_bytes(batch, heads_q, heads_kv, total_q, total_k, head_dim,
+                           qk_quant_gran="per_warp"):
+    return _lib.load().sage_attn_varlen_workspace_size(batch, heads_q, heads_kv, total_q, total_k,
+                                                       head_dim, GRAN[qk_quant_gran])
+
+
+def alloc_workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _dims(q, k, layout):
+    if layout == "HND":
+        return q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3]
+    return q.shape[0], q.shape[2], k.shape[2], q.shape[1], k.shape[1], q.shape[3]
+
+
+def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, return_lse=False,
+              qk_quant_gran="per_warp", pv_accum_dtype="fp32", smooth_k=True, smooth_v=False,
+              out=None, lse=None, workspace=None, stream=None, _debug_scores=None):
+    """Quantized attention forward. q: [B, Hq, Nq, d] (HND) or [B, Nq, Hq, d] (NHD);
+    k, v: [B, Hkv, Nk, d] / [B, Nk, Hkv, d]; fp16 or bf16 on one CUDA device.
+    Returns out (same shape/layout/dtype as q), plus lse [B, Hq, Nq] fp32 if return_lse."""
+    lib = _lib.load()
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
+    if not (q.is_cuda and k.device == q.device and v.device == q.device):
+        raise ValueError("q, k, v must be on one CUDA device")
+    B, Hq, Hkv, Nq, Nk, d = _dims(q, k, tensor_layout)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    need = lib.sage_attn_workspace_size(B, Hq, Hkv, Nq, Nk, d, GRAN[qk_quant_gran])
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    scale = float("nan") if sm_scale is None else float(sm_scale)
+    args = [ctypes.byref(_tensor(q)), ctypes.byref(_tensor(k)), ctypes.byref(_tensor(v)),
+            ctypes.byref(_tensor(out)), ctypes.c_void_p(lse.data_ptr() if return_lse else 0),
+            B, Hq, Hkv, Nq, Nk, d, DTYPE[q.dtype], LAYOUT[tensor_layout], int(bool(is_causal)),
+            scale, int(bool(return_lse)), GRAN[qk_quant_gran], ACC[pv_accum_dtype],
+            int(bool(smooth_k)), int(bool(smooth_v)), ctypes.c_void_p(workspace.data_ptr()),
+            workspace.numel()]
+    with torch.cuda.device(q.device):
+        if _debug_scores is None:
+            st = lib.sage_attn(*args, _stream_ptr(stream))
+        else:
+            st = lib.sage_attn_debug_scores(*args, ctypes.c_void_p(_debug_scores.data_ptr()),
+                                            _stream_ptr(stream))
+    _check(st, "sage_attn")
+    return (out, lse) if return_lse else out
+
+
+def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                     is_causal=False, sm_scale=None, return_lse=False, qk_quant_gran="per_warp",
+                     pv_accum_dtype="fp32", smooth_k=True, smooth_v=False, out=None, lse=None,
+                     workspace=None, stream=None):
+    """Variable-length forward: q [Tq, Hq, d], k/v [Tk, Hkv, d], cu_seqlens int32 [B+1] on the
+    device. Returns out [Tq, Hq, d] (+ lse [Hq, Tq] fp32 if return_lse)."""
+    lib = _lib.load()
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    Tq, Hq, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    need = lib.sage_attn_varlen_workspace_size(B, Hq, Hkv, Tq, Tk, d, GRAN[qk_quant_gran])
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    scale = float("nan") if sm_scale is None else float(sm_scale)
+    with torch.cuda.device(q.device):
+        st = lib.sage_attn_varlen(
+            ctypes.byref(_packed(q)), ctypes.byref(_packed(k)), ctypes.byref(_packed(v)),
+            ctypes.byref(_packed(out)), ctypes.c_void_p(lse.data_ptr() if return_lse else 0),
+            ctypes.c_void_p(cu_seqlens_q.data_ptr()), ctypes.c_void_p(cu_seqlens_k.data_ptr()),
+            B, int(max_seqlen_q), int(max_seqlen_k), Tq, Tk, Hq, Hkv, d, DTYPE[q.dtype],
+            int(bool(is_causal)), scale, int(bool(return_lse)), GRAN[qk_quant_gran],
+            ACC[pv_accum_dtype], int(bool(smooth_k)), int(bool(smooth_v)),
+            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    _check(st, "sage_attn_varlen")
+    return (out, lse) if return_lse else out
+
+
+def read_device_status(workspace, stream=None):
+    return _lib.load().sage_read_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream_ptr(stream))
+
+
+def export_quant(workspace, B, Hq, Hkv, Nq, Nk, d, qk_quant_gran, stream=None):
+    """Copies the quantised tensors a previous dense sage_attn left in `workspace`."""
+    lib = _lib.load()
+    g = GRAN[qk_quant_gran]
+    gq, gk = {0: (128, 64), 1: (32, 64), 2: (1, 16)}[g]
+    dev = workspace.device
+    res = dict(
+        q8=torch.empty((B, Hq, Nq, d), dtype=torch.int8, device=dev),
+        sq=torch.empty((B, Hq, -(-Nq // gq)), dtype=torch.float32, device=dev),
+        k8=torch.empty((B, Hkv, Nk, d), dtype=torch.int8, device=dev),
+        sk=torch.empty((B, Hkv, -(-Nk // gk)), dtype=torch.float32, device=dev),
+        kmean=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev),
+        vmean=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev),
+        vscale=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev),
+        v8=torch.empty((B, Hkv, Nk, d), dtype=torch.uint8, device=dev),
+    )
+    order = ["q8", "sq", "k8", "sk", "kmean", "vmean", "vscale", "v8"]
+    st = lib.sage_debug_export_quant(ctypes.c_void_p(workspace.data_ptr()), B, Hq, Hkv, Nq, Nk, d, g,
+                                     *[ctypes.c_void_p(res[n].data_ptr()) for n in order],
+                                     _stream_ptr(stream))
+    _check(st, "sage_debug_export_quant")
+    return res
+
+
+def e4m3(x, stream=None):
+    """FP8 E4M3 conversion with the kernels' rounding (test hook): float32 CUDA -> uint8."""
+    lib = _lib.load()
+    x = x.contiguous()
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib.sage_debug_e4m3(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                               x.numel(), _stream_ptr(stream)), "sage_debug_e4m3")
+    return out
+
+
+def profile_enable(on=True):
+    _check(_lib.load().sage_profile_enable(int(bool(on))), "sage_profile_enable")
+
+
+def profile_read():
+    """Summed ms per stage [stats, quant, attention] of the calls since enable / last read."""
+    ms = (ctypes.c_double * 3)()
+    n = ctypes.c_int(0)
+    _check(_lib.load().sage_profile_read(ms, ctypes.byref(n)), "sage_profile_read")
+    return list(ms), n.value
+
+
+def default_sm_scale(head_dim):
+    return 1.0 / math.sqrt(head_dim)
+
+
+__all__ = ["sage_attn", "sage_attn_varlen", "SageError", "workspace_bytes",
+           "varlen_workspace_bytes", "alloc_workspace", "read_device_status", "export_quant", "e4m3",
+           "profile_enable", "profile_read"]

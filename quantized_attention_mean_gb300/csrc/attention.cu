@@ -1,0 +1,445 @@
+// Stage 3 of the method (pwwt.cn "SageAttention deployment pitfalls guide" §1, §4.1, §4.2;
+// pnsm.cn "SageAttention on AMD 9070 XT without the HIP SDK" §2: FlashAttention-style
+// tiling with a quantisation layer): a fused, warp-specialised attention kernel for sm_103a.
+//
+// One CTA owns two 128-row query tiles (A and B) of one (sequence, query head) and walks the
+// KV tiles of 128 keys:
+//   warp 8      TMA producer: Q tiles once, then K tiles (integer-valued fp16 codes) and
+//               V^T tiles (E4M3) through a ring of shared-memory stages;
+//   warp 9      allocates tensor memory and issues the MMAs from one thread:
+//               S = Q8 . K8^T  (tcgen05 kind::f16 on the INT8 codes: every product and partial
+//                               sum is an integer below 2^24, so the fp32 accumulator holds
+//                               the exact INT32 score),
+//               O += P~ . V~   (tcgen05 kind::f8f6f4, E4M3 x E4M3 -> fp32 in tensor memory);
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread per query row
+//               reads its S row from tensor memory, dequantises (s_q . s_k . sm_scale),
+//               masks, keeps the running max / sum, writes P~ = e4m3(2^(x - m) . sigma_P) to
+//               shared memory, rescales its O row in tensor memory when the max grows, and
+//               finally writes O = acc . s_v / l + v_mean and the LSE.
+// The two tiles ping-pong: while one tile's softmax runs, the tensor core computes the other
+// tile's scores. Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+//
+// Every wait is bounded; a timeout records SAGE_ERR_TIMEOUT and all roles exit cleanly.
+#include "launch.h"
+#include "problem.cuh"
+#include "sm103_ptx.cuh"
+
+namespace sage {
+
+constexpr int kAttnThreads = 320;  // 10 warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int DP>
+struct AttnCfg {
+  static constexpr int kChunks = DP / 64;                       // 128-byte K-chunks of a row
+  static constexpr int kQTileBytes = kTileRows * DP * 2;        // fp16 codes
+  static constexpr int kKTileBytes = kTileKeys * DP * 2;
+  static constexpr int kVTileBytes = DP * kTileKeys;            // E4M3, V^T
+  static constexpr int kPTileBytes = kTileRows * kTileKeys;     // E4M3
+  static constexpr int kKStages = DP == 128 ? 2 : 3;
+  static constexpr int kVStages = DP == 128 ? 2 : 3;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
+  static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64;
+  // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
+  static constexpr int kSmem = (kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024);
+};
+
+// Instruction descriptors: M = 128 rows, fp32 accumulate, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_qk() { return make_idesc(1, 0, 0, 128, 128); }
+template <int DP>
+__host__ __device__ constexpr uint32_t idesc_pv() { return make_idesc(1, 0, 0, 128, DP); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int DP>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const Problem p) {
+  using C = AttnCfg<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = sm + C::kOffQ;
+  uint8_t* sK = sm + C::kOffK;
+  uint8_t* sV = sm + C::kOffV;
+  uint8_t* sP = sm + C::kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::kKStages;
+  uint64_t* v_full = k_empty + C::kKStages;
+  uint64_t* v_empty = v_full + C::kVStages;
+  uint64_t* s_full = v_empty + C::kVStages;  // [2]
+  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* o_full = p_full + 2;             // [2]
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: (query head, 256-row pair, sequence); heaviest pairs first when causal
+  const int h = blockIdx.x;
+  const int b = p.varlen ? p.seqinfo[kSiOrder * p.batch + blockIdx.z] : blockIdx.z;
+  const Seq s = get_seq(p, b);
+  const int npairs_seq = (s.len_q + 2 * kTileRows - 1) / (2 * kTileRows);
+  const int pair = p.is_causal ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)blockIdx.y;
+  if (pair >= npairs_seq || s.len_k <= 0) return;  // uniform across the CTA
+  const int q_start = pair * 2 * kTileRows;
+  const int rows_a = min(kTileRows, s.len_q - q_start);
+  const int rows_b = max(0, min(kTileRows, s.len_q - q_start - kTileRows));
+  const bool has_b = rows_b > 0;
+  const int hk = h / (p.hq / p.hkv);
+  const int64_t plane_q = plane_of(p, b, h, p.hq);
+  const int64_t plane_kv = plane_of(p, b, hk, p.hkv);
+  int kv_end = s.len_k;
+  if (p.is_causal) kv_end = min(kv_end, q_start + (has_b ? kTileRows + rows_b : rows_a));
+  const int n_tiles = (kv_end + kTileKeys - 1) / kTileKeys;
+
+  // ---- set-up: barriers, tensor memory
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+    for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_full[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // =========================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int qrow = s.row0_q + q_start;
+      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::kQTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(sQ + c * kTileRows * 128, &tmQ, q_full, c * 64, qrow, (int)plane_q);
+        if (has_b)
+          tma_load_3d(sQ + C::kQTileBytes + c * kTileRows * 128, &tmQ, q_full, c * 64,
+                      qrow + kTileRows, (int)plane_q);
+      }
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int krow = s.row0_k + j * kTileKeys;
+        const int st = j % C::kKStages;
+        if (j >= C::kKStages) ok = mbar_wait(&k_empty[st], ((j / C::kKStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&k_full[st], C::kKTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sK + st * C::kKTileBytes + c * kTileKeys * 128, &tmK, &k_full[st], c * 64,
+                      krow, (int)plane_kv);
+        ++issued_k;
+        const int sv = j % C::kVStages;
+        if (j >= C::kVStages) ok = mbar_wait(&v_empty[sv], ((j / C::kVStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
+        tma_load_3d(sV + sv * C::kVTileBytes, &tmV, &v_full[sv], krow, 0, (int)plane_kv);
+        ++issued_v;
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA's shared memory goes away
+        volatile int never = 0;
+        mbar_wait(q_full, 0, &never);
+        for (int j = max(0, issued_k - C::kKStages); j < issued_k; ++j)
+          mbar_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1, &never);
+        for (int j = max(0, issued_v - C::kVStages); j < issued_v; ++j)
+          mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, &never);
+        record_error(p.err, kDevTimeout);
+      }
+    }
+  } else if (warp == 9) {
+    // =========================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t sq_addr = smem_u32(sQ), sk_addr = smem_u32(sK), sv_addr = smem_u32(sV),
+                     sp_addr = smem_u32(sP);
+      const int nx = has_b ? 2 : 1;
+      auto issue_qk = [&](int x, int st) {
+        const uint32_t qa = sq_addr + x * C::kQTileBytes, ka = sk_addr + st * C::kKTileBytes;
+#pragma unroll
+        for (int k = 0; k < DP / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kTileRows * 128) + (k & 3) * 32;
+          mma_f16_ss(tmem + (x ? 128u : 0u), sdesc_sw128(qa + off), sdesc_sw128(ka + off), idesc_qk(), k > 0);
+        }
+        mma_commit(&s_full[x]);
+      };
+      auto issue_pv = [&](int x, int sv, bool first) {
+        const uint32_t pa = sp_addr + x * C::kPTileBytes, va = sv_addr + sv * C::kVTileBytes;
+#pragma unroll
+        for (int k = 0; k < kTileKeys / 32; ++k)
+          mma_f8_ss(tmem + (x ? 384u : 256u), sdesc_sw128(pa + k * 32), sdesc_sw128(va + k * 32), idesc_pv<DP>(),
+                    (!first || k > 0) ? 1u : 0u);
+        mma_commit(&o_full[x]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(&k_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < nx; ++x) issue_qk(x, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int sv = j % C::kVStages;
+        const int nst = (j + 1) % C::kKStages;
+        for (int x = 0; x < nx && ok; ++x) {
+          ok = mbar_wait(&p_full[x], j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (j + 1 < n_tiles) {
+            if (x == 0) ok = mbar_wait(&k_full[nst], ((j + 1) / C::kKStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(x, nst);
+          }
+          if (x == 0) ok = mbar_wait(&v_full[sv], (j / C::kVStages) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(x, sv, j == 0);
+        }
+        if (!ok) break;
+        if (j + 1 < n_tiles) mma_commit(&k_empty[nst]);
+        mma_commit(&v_empty[sv]);
+      }
+      // every MMA must have finished before tensor memory is released
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never);
+      if (!ok) record_error(p.err, kDevTimeout);
+    }
+  } else {
+    // =========================================================== softmax (warps 0-7)
+    const int x = warp >> 2;               // tile A or B
+    const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x == 0 ? 0u : 128u);
+    const uint32_t tO = tmem + lane_base + (x == 0 ? 256u : 384u);
+    uint8_t* my_p = sP + x * C::kPTileBytes + r * 128;
+    const int xrows = x == 0 ? rows_a : rows_b;
+    const bool active_tile = x == 0 || has_b;
+    const int i = q_start + x * kTileRows + r;  // query row within the sequence
+    const bool row_valid = active_tile && r < xrows;
+    const float log2_sigma = p.acc_mode == 1 ? 0.0f : 8.807354922057604f;  // log2(448)
+    float sq = 0.f;
+    if (row_valid) sq = __ldg(&p.sq[plane_q * p.sq_pp + (s.row0_q + i) / p.gq]);
+    const float row_scale = sq * p.sm_scale * kLog2e;
+    const float* skp = p.sk + plane_kv * p.sk_pp + s.row0_k / p.gk;
+    const int gk = p.gk;
+    float m = __int_as_float(0xff800000);  // running max (log2 units)
+    float l = 0.f;                          // running sum of 2^(x - m) * sigma
+    bool ok = true;
+    if (active_tile) {
+      for (int j = 0; j < n_tiles; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+        tmem_ld32(tS + 0, sr[0]);
+        tmem_ld32(tS + 32, sr[1]);
+        tmem_ld32(tS + 64, sr[2]);
+        tmem_ld32(tS + 96, sr[3]);
+        tmem_wait_ld(sr[0]);
+        tmem_wait_ld(sr[1]);
+        tmem_wait_ld(sr[2]);
+        tmem_wait_ld(sr[3]);
+        const int kv0 = j * kTileKeys;
+        if (p.dbg_scores != nullptr && row_valid) {
+          int32_t* dst = p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (kv0 + c < s.len_k) dst[kv0 + c] = __float2int_rn(__uint_as_float(sr[c >> 5][c & 31]));
+        }
+        // multipliers c_g = s_q * s_k * sm_scale * log2(e) for the 8 sub-groups of 16 keys
+        // (a K scale group is 16 or 64 keys, so each sub-group has one scale)
+        float cg[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int kg = kv0 + g * 16;
+          cg[g] = kg < s.len_k ? row_scale * __ldg(&skp[kg / gk]) : 0.f;
+        }
+        const bool need_mask = (kv0 + kTileKeys > s.len_k) ||
+                               (p.is_causal && kv0 + kTileKeys - 1 > q_start + x * kTileRows);
+        float tile_max = __int_as_float(0xff800000);
+        if (!need_mask) {
+          // max of the raw integer scores per sub-group, then scaled (c_g >= 0 keeps order)
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float mg = __uint_as_float(sr[g >> 1][(g & 1) * 16]);
+#pragma unroll
+            for (int c = 1; c < 16; ++c) mg = fmaxf(mg, __uint_as_float(sr[g >> 1][(g & 1) * 16 + c]));
+            tile_max = fmaxf(tile_max, mg * cg[g]);
+          }
+        } else {
+          // masked tile: scale each score; -inf where the key is past the end or causal-masked
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int kj = kv0 + c;
+            const bool allowed = kj < s.len_k && (!p.is_causal || kj <= i);
+            const float t = allowed ? __uint_as_float(sr[c >> 5][c & 31]) * cg[c >> 4]
+                                    : __int_as_float(0xff800000);
+            sr[c >> 5][c & 31] = __float_as_uint(t);
+            tile_max = fmaxf(tile_max, t);
+          }
+        }
+        const float m_new = fmaxf(m, tile_max);
+        const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
+        const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
+        const float bias = log2_sigma - m_use;
+        // P~ = e4m3(2^(x - m) * sigma), packed 4 per word, and the row sum
+        uint32_t pk[32];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float sv = __uint_as_float(sr[(c + u) >> 5][(c + u) & 31]);
+            e[u] = need_mask ? ex2(sv + bias) : ex2(fmaf(sv, cg[(c + u) >> 4], bias));
+            rs += e[u];
+          }
+          pk[c / 4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
+        }
+        l = l * alpha + rs;
+        m = m_new;
+        // P tile buffer and O are free once the previous P.V of this tile has completed
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 val = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+          *reinterpret_cast<uint4*>(my_p + ((ch ^ (r & 7)) << 4)) = val;
+        }
+        fence_proxy_async_smem();
+        if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
+#pragma unroll
+          for (int cc = 0; cc < DP / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(tO + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+      }
+      // ---- epilogue
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (n_tiles - 1) & 1, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const float* vsc = p.vscale + ((int64_t)b * p.hkv + hk) * p.d;
+        const float* vmn = p.vmean + ((int64_t)b * p.hkv + hk) * p.d;
+        const int64_t orow = (int64_t)b * p.o_sb + (int64_t)(s.tok0_q + i) * p.o_sn + (int64_t)h * p.o_sh;
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld(o);
+          if (row_valid && cc * 32 < p.d) {
+            float v[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              const int c = cc * 32 + u;
+              v[u] = c < p.d ? fmaf(__uint_as_float(o[u]) * __ldg(&vsc[c]), inv_l, __ldg(&vmn[c])) : 0.f;
+            }
+            if (p.dtype == 0) {
+              __half* dst = static_cast<__half*>(p.o) + orow + cc * 32;
+              if (p.vec16 && cc * 32 + 32 <= p.d) {
+#pragma unroll
+                for (int u = 0; u < 32; u += 8) {
+                  __align__(16) __half2 hv[4];
+#pragma unroll
+                  for (int w = 0; w < 4; ++w) hv[w] = __floats2half2_rn(v[u + 2 * w], v[u + 2 * w + 1]);
+                  *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
+                }
+              } else {
+                for (int u = 0; u < 32 && cc * 32 + u < p.d; ++u) dst[u] = __float2half_rn(v[u]);
+              }
+            } else {
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + orow + cc * 32;
+              if (p.vec16 && cc * 32 + 32 <= p.d) {
+#pragma unroll
+                for (int u = 0; u < 32; u += 8) {
+                  __align__(16) __nv_bfloat162 hv[4];
+#pragma unroll
+                  for (int w = 0; w < 4; ++w) hv[w] = __floats2bfloat162_rn(v[u + 2 * w], v[u + 2 * w + 1]);
+                  *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
+                }
+              } else {
+                for (int u = 0; u < 32 && cc * 32 + u < p.d; ++u) dst[u] = __float2bfloat16_rn(v[u]);
+              }
+            }
+          }
+        }
+        if (p.return_lse && row_valid) {
+          float lse = (m + __log2f(l) - log2_sigma) * 0.6931471805599453f;
+          if (p.smooth_k) lse += p.sm_scale * p.qkc[plane_q * p.q_rows + s.row0_q + i];
+          const int64_t li = p.varlen ? (int64_t)h * p.lse_plane + s.tok0_q + i
+                                      : ((int64_t)b * p.hq + h) * p.nq + i;
+          p.lse[li] = lse;
+        }
+      }
+      if (!ok) record_error(p.err, kDevTimeout);
+    }
+  }
+
+  // ---- teardown: every role is done with tensor memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+size_t attention_smem_bytes(int dp) { return dp == 64 ? AttnCfg<64>::kSmem : AttnCfg<128>::kSmem; }
+
+cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
+                             cudaStream_t stream) {
+  const dim3 grid(p.hq, grid_pairs, p.batch);
+  if (p.dp == 64) {
+    constexpr int smem = AttnCfg<64>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_kernel<64><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  } else {
+    constexpr int smem = AttnCfg<128>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_kernel<128><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sage

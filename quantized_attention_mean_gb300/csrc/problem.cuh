@@ -1,0 +1,120 @@
+// Problem descriptor shared by the host API and the kernels, the workspace layout, and the
+// small device helpers (input loads, per-sequence geometry, FP8 packing, error recording).
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace sage {
+
+constexpr int kTileRows = 128;   // query rows per attention tile, tokens per quantisation tile
+constexpr int kTileKeys = 128;   // keys per attention KV tile
+constexpr int kStatsChunk = 512; // tokens per block in the K/V statistics pass
+
+// Device-side status codes (mirror sage_status in include/sageattn.h).
+enum DevStatus : int { kDevOk = 0, kDevRange = 7, kDevTimeout = 9, kDevSeqlens = 12 };
+
+// Everything the kernels need. Strides are in elements; offset of (seq b, token t, head h)
+// in an input/output tensor is b*s_b + (tok0(b) + t)*s_n + h*s_h, where tok0 = 0 for dense
+// problems and cu_seqlens[b] for varlen (whose s_b is 0).
+struct Problem {
+  int batch, hq, hkv, d, dp;       // dp: padded head_dim (64 or 128)
+  int nq, nk;                      // dense: sequence lengths; varlen: max lengths
+  int varlen, dtype, is_causal, return_lse, smooth_k, smooth_v;
+  int gq, gk;                      // token-group sizes of Q and K scales
+  int acc_mode;                    // 0: fp32 (P scaled by 448), 1: fp16 partials + fp32
+  int vec16;                       // inputs allow 16-byte vector loads
+  float sm_scale;
+  float range_limit;               // smallest float >= 2^38 / N (dense only; varlen per seq)
+  const void* q; int64_t q_sb, q_sh, q_sn;
+  const void* k; int64_t k_sb, k_sh, k_sn;
+  const void* v; int64_t v_sb, v_sh, v_sn;
+  void* o;       int64_t o_sb, o_sh, o_sn;
+  float* lse;                      // dense [B,Hq,Nq]; varlen [Hq,total_q]
+  int64_t lse_plane;               // varlen: total_q
+  const int* cu_q; const int* cu_k;
+  int total_q, total_k;
+  // workspace
+  int* err;
+  long long* ksum; long long* vsum; int* vmin; int* vmax;   // [batch*hkv*d]
+  float* kmean; float* vmean; float* vscale;                  // [batch*hkv*d]
+  __half* qc; __half* kc; uint8_t* vt;                        // codes
+  float* sq; float* sk; float* qkc;                           // scales, LSE correction
+  int* seqinfo;                    // varlen: [5][batch] tok0_q,len_q,row0_q,tok0_k,len_k,row0_k...
+  int64_t q_rows, k_rows;          // rows per plane in qc / kc (dense: nq / nk)
+  int64_t vt_pitch;                // bytes per channel row of vt
+  int64_t sq_pp, sk_pp;            // scale groups per plane
+  int32_t* dbg_scores;             // optional exact-score dump [B,Hq,Nq,Nk]
+};
+
+struct Seq {
+  int tok0_q, len_q, row0_q, tok0_k, len_k, row0_k;
+};
+
+// varlen seqinfo rows (each of length batch)
+enum { kSiTok0Q = 0, kSiLenQ, kSiRow0Q, kSiTok0K, kSiLenK, kSiRow0K, kSiOrder, kSiRows };
+
+__device__ __forceinline__ Seq get_seq(const Problem& p, int b) {
+  Seq s;
+  if (!p.varlen) {
+    s.tok0_q = 0; s.len_q = p.nq; s.row0_q = 0;
+    s.tok0_k = 0; s.len_k = p.nk; s.row0_k = 0;
+  } else {
+    const int* si = p.seqinfo;
+    const int B = p.batch;
+    s.tok0_q = si[kSiTok0Q * B + b]; s.len_q = si[kSiLenQ * B + b]; s.row0_q = si[kSiRow0Q * B + b];
+    s.tok0_k = si[kSiTok0K * B + b]; s.len_k = si[kSiLenK * B + b]; s.row0_k = si[kSiRow0K * B + b];
+  }
+  return s;
+}
+
+// Plane index of (sequence b, head h) in the code/scale arrays.
+__device__ __forceinline__ int64_t plane_of(const Problem& p, int b, int h, int heads) {
+  return p.varlen ? (int64_t)h : (int64_t)b * heads + h;
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+// Loads channels [c0, c0+8) of one row; channels >= d read as 0.
+template <typename T>
+__device__ __forceinline__ void load8(const T* row, int c0, int d, int vec16, float (&x)[8]) {
+  if (vec16 && c0 + 8 <= d) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(row + c0));
+    const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = to_f32<T>(h[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = (c0 + i < d) ? to_f32<T>(row[c0 + i]) : 0.0f;
+  }
+}
+
+// Two floats -> two E4M3 bytes (RNE, saturate to +-448): byte 0 = lo, byte 1 = hi.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Order-preserving float <-> int map for atomicMin / atomicMax on floats.
+__device__ __forceinline__ int float_to_ordered(float f) {
+  int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float ordered_to_float(int i) {
+  return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF);
+}
+
+// Exact, order-free mean from the fixed-point sum: fl32(fl64(fl64(S) * 2^-24 / n)).
+__device__ __forceinline__ float fixed_point_mean(long long s, int n) {
+  double m = __dmul_rn(__ll2double_rn(s), 5.9604644775390625e-08);  // * 2^-24, exact
+  return __double2float_rn(__ddiv_rn(m, (double)n));
+}
+
+}  // namespace sage

@@ -1,0 +1,455 @@
+// Stages 1-2 of the method (pwwt.cn "SageAttention deployment pitfalls guide" §1, §4.2):
+// smoothing statistics for K and V, INT8 quantisation of Q and K with per-token-group
+// scales, and per-channel FP8 E4M3 quantisation of V.
+//
+// Both kernels are HBM-bound streaming passes: each block walks a tile of tokens with
+// 16-byte vector loads (8 channels per thread, 16 threads per token row), reduces with
+// warp shuffles and shared memory, and writes coalesced outputs.
+//
+// Bit-exactness: the mean is an exact fixed-point sum (order-free, so atomics are fine);
+// scales and codes use explicitly rounded IEEE operations (__fdiv_rn, __fmul_rn, __fsub_rn,
+// __float2int_rn) so no contraction or reassociation can change a code.
+#include "launch.h"
+#include "problem.cuh"
+
+namespace sage {
+
+// ------------------------------------------------------------------------------------------
+// Varlen set-up: validate cu_seqlens and lay sequences out in 128-row aligned segments.
+// One block. Writes seqinfo (tok0, len, row0 for q and k, LPT order); invalid input
+// records kDevSeqlens and zeroes every length so later kernels do nothing.
+__global__ void __launch_bounds__(1024) varlen_setup_kernel(Problem p) {
+  const int B = p.batch;
+  int* si = p.seqinfo;
+  __shared__ int bad;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    if (p.cu_q[0] != 0 || p.cu_k[0] != 0 || p.cu_q[B] != p.total_q || p.cu_k[B] != p.total_k)
+      bad = 1;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int lq = p.cu_q[b + 1] - p.cu_q[b], lk = p.cu_k[b + 1] - p.cu_k[b];
+    if (lq < 0 || lk < 0 || lq > p.nq || lk > p.nk || (lq > 0 && lk == 0)) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int rq = 0, rk = 0;
+    for (int b = 0; b < B; ++b) {
+      const int lq = bad ? 0 : p.cu_q[b + 1] - p.cu_q[b];
+      const int lk = bad ? 0 : p.cu_k[b + 1] - p.cu_k[b];
+      si[kSiTok0Q * B + b] = bad ? 0 : p.cu_q[b];
+      si[kSiLenQ * B + b] = lq;
+      si[kSiRow0Q * B + b] = rq;
+      si[kSiTok0K * B + b] = bad ? 0 : p.cu_k[b];
+      si[kSiLenK * B + b] = lk;
+      si[kSiRow0K * B + b] = rk;
+      rq += (lq + kTileRows - 1) / kTileRows * kTileRows;
+      rk += (lk + kTileKeys - 1) / kTileKeys * kTileKeys;
+    }
+    if (bad) record_error(p.err, kDevSeqlens);
+  }
+  __syncthreads();
+  // Longest-processing-time order: sequences by decreasing len_q * len_k (stable).
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const long long w = (long long)si[kSiLenQ * B + b] * si[kSiLenK * B + b];
+    int rank = 0;
+    if (B <= 4096) {
+      for (int o = 0; o < B; ++o) {
+        const long long wo = (long long)si[kSiLenQ * B + o] * si[kSiLenK * B + o];
+        rank += (wo > w) || (wo == w && o < b);
+      }
+    } else {
+      rank = b;
+    }
+    si[kSiOrder * B + rank] = b;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Workspace reset before the statistics pass: sums to 0, min / max to +inf / -inf.
+__global__ void ws_reset_kernel(Problem p, int n_stats) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_stats; i += gridDim.x * blockDim.x) {
+    p.ksum[i] = 0;
+    p.vsum[i] = 0;
+    p.vmin[i] = float_to_ordered(__int_as_float(0x7f800000));
+    p.vmax[i] = float_to_ordered(__int_as_float(0xff800000));
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// K/V statistics: fixed-point sums of K and V (smooth_k / smooth_v) and the min / max of V
+// per (sequence, kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads:
+// thread = (row group rg in 0..15, channel vector vec in 0..15).
+template <typename T>
+__global__ void __launch_bounds__(256) kv_stats_kernel(Problem p) {
+  const int chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const Seq s = get_seq(p, b);
+  const int t0 = chunk * kStatsChunk;
+  if (t0 >= s.len_k) return;
+  const int t1 = min(t0 + kStatsChunk, s.len_k);
+  const int vec = threadIdx.x & 15, rg = threadIdx.x >> 4;
+  const int c0 = vec * 8;
+  const bool active = c0 < p.d;
+  const float lim = p.varlen ? __double2float_ru(__ddiv_rn(274877906944.0, (double)s.len_k))
+                             : p.range_limit;
+  long long ks[8], vs[8];
+  float vmn[8], vmx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ks[i] = 0; vs[i] = 0;
+    vmn[i] = __int_as_float(0x7f800000);
+    vmx[i] = __int_as_float(0xff800000);
+  }
+  bool range_bad = false;
+  const T* kp = static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh;
+  const T* vp = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
+  if (active) {
+    for (int t = t0 + rg; t < t1; t += 16) {
+      const int64_t tok = (int64_t)(s.tok0_k + t);
+      float vx[8];
+      load8<T>(vp + tok * p.v_sn, c0, p.d, p.vec16, vx);
+      if (p.smooth_k) {
+        float kx[8];
+        load8<T>(kp + tok * p.k_sn, c0, p.d, p.vec16, kx);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          range_bad |= fabsf(kx[i]) >= lim;
+          ks[i] += __float2ll_rz(kx[i] * 16777216.0f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (p.smooth_v) {
+          range_bad |= fabsf(vx[i]) >= lim;
+          vs[i] += __float2ll_rz(vx[i] * 16777216.0f);
+        }
+        vmn[i] = fminf(vmn[i], vx[i]);
+        vmx[i] = fmaxf(vmx[i], vx[i]);
+      }
+    }
+  }
+  if (range_bad) record_error(p.err, kDevRange);
+  // reduce the two row groups that share a warp, then the 8 warps through shared memory
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], 16);
+    vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], 16);
+    vmn[i] = fminf(vmn[i], __shfl_xor_sync(0xffffffffu, vmn[i], 16));
+    vmx[i] = fmaxf(vmx[i], __shfl_xor_sync(0xffffffffu, vmx[i], 16));
+  }
+  __shared__ long long red_s[8][128];
+  __shared__ float red_f[8][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t sidx = ((int64_t)b * p.hkv + hk) * p.d;
+  // pass 1: K sums
+  if (lane < 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = ks[i];
+  }
+  __syncthreads();
+  if (p.smooth_k && threadIdx.x < p.d) {
+    long long acc = 0;
+    for (int w = 0; w < 8; ++w) acc += red_s[w][threadIdx.x];
+    atomicAdd(reinterpret_cast<unsigned long long*>(&p.ksum[sidx + threadIdx.x]),
+              static_cast<unsigned long long>(acc));
+  }
+  __syncthreads();
+  // pass 2: V sums
+  if (lane < 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = vs[i];
+  }
+  __syncthreads();
+  if (p.smooth_v && threadIdx.x < p.d) {
+    long long acc = 0;
+    for (int w = 0; w < 8; ++w) acc += red_s[w][threadIdx.x];
+    atomicAdd(reinterpret_cast<unsigned long long*>(&p.vsum[sidx + threadIdx.x]),
+              static_cast<unsigned long long>(acc));
+  }
+  // pass 3: V min
+  if (lane < 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmn[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < p.d) {
+    float m = red_f[0][threadIdx.x];
+    for (int w = 1; w < 8; ++w) m = fminf(m, red_f[w][threadIdx.x]);
+    atomicMin(&p.vmin[sidx + threadIdx.x], float_to_ordered(m));
+  }
+  __syncthreads();
+  // pass 4: V max
+  if (lane < 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmx[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < p.d) {
+    float m = red_f[0][threadIdx.x];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red_f[w][threadIdx.x]);
+    atomicMax(&p.vmax[sidx + threadIdx.x], float_to_ordered(m));
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Quantisation. Grid: (128-token tiles, Hq + 2*Hkv, batch); blockIdx.y selects Q head,
+// K head or V head. 256 threads; thread (rg, vec) holds rows rg + 16*i (i < 8), channels
+// [8*vec, 8*vec + 8).
+//   Q: codes = INT8 per group of gq rows (stored as integer-valued fp16 for the tensor
+//      cores), scales sq, and (return_lse with smooth_k) the LSE term q . kmean.
+//   K: K' = K - kmean, INT8 per group of gk rows.
+//   V: V' = V - vmean, E4M3 with the per-channel scale absmax/448, written transposed
+//      [channel][token] so that P.V reads V^T tiles K-major.
+// Rows past the sequence end up to the stored tile end are written as zeros.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_kernel(Problem p) {
+  const int tile = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
+  const int kind = y < p.hq ? 0 : (y < p.hq + p.hkv ? 1 : 2);
+  const int h = kind == 0 ? y : (kind == 1 ? y - p.hq : y - p.hq - p.hkv);
+  const Seq s = get_seq(p, b);
+  const int len = kind == 0 ? s.len_q : s.len_k;
+  // rows stored for this sequence: dense planes hold exactly len rows; varlen segments are
+  // padded to a multiple of 128
+  const int stored = p.varlen ? (len + kTileRows - 1) / kTileRows * kTileRows : len;
+  const int r0 = tile * kTileRows;
+  if (r0 >= stored) return;
+  const int vec = threadIdx.x & 15, rg = threadIdx.x >> 4;
+  const int c0 = vec * 8;
+  const int d = p.d, dp = p.dp;
+  const int hk = kind == 0 ? y / (p.hq / p.hkv) : h;   // kv head feeding this q head
+  const int64_t sidx = ((int64_t)b * p.hkv + hk) * d;
+
+  __shared__ float rowmax[kTileRows];
+  __shared__ float grcp[kTileRows];
+  __shared__ __align__(16) uint8_t vtile[128][kTileRows + 16];
+
+  // per-channel offsets: smoothing means (and for V the scale reciprocal)
+  float mean[8], rcpv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { mean[i] = 0.f; rcpv[i] = 0.f; }
+  const bool smooth = kind == 1 ? p.smooth_k : (kind == 2 ? p.smooth_v : false);
+  if (kind != 0 && c0 < d) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + i < d && smooth)
+        mean[i] = fixed_point_mean(kind == 1 ? p.ksum[sidx + c0 + i] : p.vsum[sidx + c0 + i],
+                                   s.len_k);
+  }
+  float kmean_q[8];   // for the Q-side LSE term
+#pragma unroll
+  for (int i = 0; i < 8; ++i) kmean_q[i] = 0.f;
+  const bool want_qkc = kind == 0 && p.return_lse && p.smooth_k;
+  if (want_qkc && c0 < d) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + i < d) kmean_q[i] = fixed_point_mean(p.ksum[sidx + c0 + i], s.len_k);
+  }
+  if (kind == 2 && c0 < d) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c0 + i < d) {
+        const float mx = __fsub_rn(ordered_to_float(p.vmax[sidx + c0 + i]), mean[i]);
+        const float mn = __fsub_rn(ordered_to_float(p.vmin[sidx + c0 + i]), mean[i]);
+        const float amax = fmaxf(fabsf(mx), fabsf(mn));
+        rcpv[i] = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+        if (tile == 0) {
+          p.vscale[sidx + c0 + i] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
+          p.vmean[sidx + c0 + i] = mean[i];
+        }
+      }
+    }
+  }
+  if (kind == 1 && tile == 0 && c0 < d) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + i < d) p.kmean[sidx + c0 + i] = mean[i];
+  }
+
+  // load the tile (values past the sequence end and channels past d are 0), smoothed
+  const T* base;
+  int64_t sn;
+  if (kind == 0) {
+    base = static_cast<const T*>(p.q) + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh; sn = p.q_sn;
+  } else if (kind == 1) {
+    base = static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)h * p.k_sh; sn = p.k_sn;
+  } else {
+    base = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)h * p.v_sh; sn = p.v_sn;
+  }
+  const int tok0 = kind == 0 ? s.tok0_q : s.tok0_k;
+  float x[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + rg + 16 * i;
+    if (r < len && c0 < d) {
+      load8<T>(base + (int64_t)(tok0 + r) * sn, c0, d, p.vec16, x[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[i][j] = (c0 + j < d) ? __fsub_rn(x[i][j], mean[j]) : 0.f;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
+    }
+  }
+
+  if (kind == 2) {
+    // ---- V: E4M3 codes, transposed through shared memory
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = rg + 16 * i;
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const uint32_t two = pack_e4m3x2(__fmul_rn(x[i][j], rcpv[j]), __fmul_rn(x[i][j + 1], rcpv[j + 1]));
+        if (c0 + j < dp) {
+          vtile[c0 + j][rr] = static_cast<uint8_t>(two & 0xFF);
+          vtile[c0 + j + 1][rr] = static_cast<uint8_t>(two >> 8);
+        }
+      }
+    }
+    __syncthreads();
+    // row c of the transposed tile = bytes [r0, r0 + 128) of channel c; write the bytes that
+    // exist in this plane's pitch (a multiple of 16), 16 bytes per thread
+    const int64_t plane = plane_of(p, b, h, p.hkv);
+    const int64_t col0 = (int64_t)s.row0_k + r0;
+    const int ncols = (int)min((int64_t)kTileRows, p.vt_pitch - col0);
+    for (int idx = threadIdx.x; idx < dp * 8; idx += 256) {
+      const int c = idx >> 3, ch = (idx & 7) * 16;
+      if (ch < ncols) {
+        uint4 val = *reinterpret_cast<const uint4*>(&vtile[c][ch]);
+        *reinterpret_cast<uint4*>(p.vt + (plane * dp + c) * p.vt_pitch + col0 + ch) = val;
+      }
+    }
+    return;
+  }
+
+  // ---- Q / K: INT8 codes per token group
+  const int gs = kind == 0 ? p.gq : p.gk;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[i][j]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+    if (vec == 0) rowmax[rg + 16 * i] = a;
+  }
+  __syncthreads();
+  const int ngroups = kTileRows / gs;
+  const int64_t plane = plane_of(p, b, h, kind == 0 ? p.hq : p.hkv);
+  const int row0 = kind == 0 ? s.row0_q : s.row0_k;
+  if (threadIdx.x < ngroups) {
+    const int g = threadIdx.x;
+    float a = 0.f;
+    for (int r = g * gs; r < (g + 1) * gs; ++r) a = fmaxf(a, rowmax[r]);
+    grcp[g] = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
+    if (r0 + g * gs < len) {
+      float* sc = kind == 0 ? p.sq : p.sk;
+      const int64_t pp = kind == 0 ? p.sq_pp : p.sk_pp;
+      sc[plane * pp + (row0 + r0) / gs + g] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+    }
+  }
+  __syncthreads();
+  __half* codes = kind == 0 ? p.qc : p.kc;
+  const int64_t rows_pp = kind == 0 ? p.q_rows : p.k_rows;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = rg + 16 * i;
+    const int r = r0 + rr;
+    const float rc = grcp[rr / gs];
+    __align__(16) __half hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int c = __float2int_rn(__fmul_rn(x[i][j], rc));
+      c = max(-127, min(127, c));
+      hv[j] = __int2half_rn(c);
+    }
+    if (c0 < dp && r < stored)
+      *reinterpret_cast<uint4*>(codes + (plane * rows_pp + row0 + r) * dp + c0) =
+          *reinterpret_cast<const uint4*>(hv);
+    if (want_qkc) {
+      float dot = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dot = fmaf(x[i][j], kmean_q[j], dot);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+      if (vec == 0 && r < len) p.qkc[plane * p.q_rows + row0 + r] = dot;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Export of the quantised state in canonical layouts (test hook).
+__global__ void export_codes_kernel(const __half* codes, int64_t rows_pp, int dp, int d,
+                                    int planes, int n, int8_t* out) {
+  const int64_t total = (int64_t)planes * n * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % d);
+    const int64_t r = (i / d) % n, pl = i / ((int64_t)d * n);
+    out[i] = static_cast<int8_t>(__half2int_rn(codes[(pl * rows_pp + r) * dp + c]));
+  }
+}
+__global__ void export_vt_kernel(const uint8_t* vt, int64_t pitch, int dp, int d, int planes,
+                                 int n, uint8_t* out) {
+  const int64_t total = (int64_t)planes * n * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % d);
+    const int64_t r = (i / d) % n, pl = i / ((int64_t)d * n);
+    out[i] = vt[(pl * dp + c) * pitch + r];
+  }
+}
+__global__ void e4m3_kernel(const float* x, uint8_t* out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = static_cast<uint8_t>(pack_e4m3x2(x[i], 0.f) & 0xFF);
+}
+
+// ------------------------------------------------------------------------------------------
+// Host launchers (all on the caller's stream).
+cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st) {
+  varlen_setup_kernel<<<1, 1024, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st) {
+  const int blocks = max(1, min(1024, (n_stats + 255) / 256));
+  ws_reset_kernel<<<blocks, 256, 0, st>>>(p, n_stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
+  const dim3 grid((max_len_k + kStatsChunk - 1) / kStatsChunk, p.hkv, p.batch);
+  if (p.dtype == 0) kv_stats_kernel<__half><<<grid, 256, 0, st>>>(p);
+  else kv_stats_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const Problem& p, int max_len, cudaStream_t st) {
+  const dim3 grid((max_len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
+  if (p.dtype == 0) quant_kernel<__half><<<grid, 256, 0, st>>>(p);
+  else quant_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, int d, int planes,
+                                int n, int8_t* out, cudaStream_t st) {
+  export_codes_kernel<<<1024, 256, 0, st>>>(codes, rows_pp, dp, d, planes, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_vt(const uint8_t* vt, int64_t pitch, int dp, int d, int planes, int n,
+                             uint8_t* out, cudaStream_t st) {
+  export_vt_kernel<<<1024, 256, 0, st>>>(vt, pitch, dp, d, planes, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3(const float* x, uint8_t* out, int64_t n, cudaStream_t st) {
+  e4m3_kernel<<<1024, 256, 0, st>>>(x, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace sage

@@ -1,0 +1,49 @@
+"""Shared test helpers: run the CUDA path and the oracle on the same seeded inputs."""
+
+import numpy as np
+import torch
+
+from quantized_attention_mean_gb300.workloads import ACC, GRAN, Workload, dense_inputs, to_hnd_f32
+
+TOL_MAX_ABS = 2e-2      # O vs the oracle's quantised emulation (max-abs)
+TOL_COS = 0.9995        # O vs the oracle's quantised emulation (cosine)
+TOL_COS_FP64 = 0.99     # O vs float64 unquantised attention (cosine)
+TOL_LSE = 2e-2          # LSE vs the oracle (absolute)
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+
+
+def oracle_kw(w: Workload, sm_scale=None):
+    return dict(is_causal=w.is_causal, sm_scale=sm_scale, gran=GRAN[w.gran], accum=ACC[w.accum],
+                smooth_k=w.smooth_k, smooth_v=w.smooth_v)
+
+
+def gpu_kw(w: Workload):
+    return dict(tensor_layout=w.layout, is_causal=w.is_causal, return_lse=w.return_lse,
+                qk_quant_gran=w.gran, pv_accum_dtype=w.accum, smooth_k=w.smooth_k,
+                smooth_v=w.smooth_v)
+
+
+def run_gpu_dense(w: Workload, q, k, v, sm_scale=None, debug_scores=False):
+    import quantized_attention_mean_gb300 as qa
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    B, Hq, Hkv, Nq, Nk, d = w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d
+    ws = qa.alloc_workspace(qa.workspace_bytes(B, Hq, Hkv, Nq, Nk, d, w.gran), dev)
+    scores = None
+    if debug_scores:
+        scores = torch.full((B, Hq, Nq, Nk), -2**31, dtype=torch.int32, device=dev)
+    res = qa.sage_attn(qd, kd, vd, sm_scale=sm_scale, workspace=ws, _debug_scores=scores, **gpu_kw(w))
+    out, lse = res if w.return_lse else (res, None)
+    torch.cuda.synchronize()
+    status = qa.read_device_status(ws)
+    return dict(out=out, lse=lse, ws=ws, scores=scores, status=status)
+
+
+def out_to_hnd(out, layout):
+    o = out.float().cpu()
+    return (o.transpose(1, 2) if layout == "NHD" else o).numpy()

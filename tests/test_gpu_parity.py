@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+Bit-exact: INT8 Q/K codes and their scales, the smoothing means, FP8 V codes and scales,
+and the integer scores S = Q8·K8^T as the attention kernel reads them from tensor memory.
+Tolerance: O within max-abs 2e-2 and cosine >= 0.9995 of the oracle's quantised emulation,
+cosine >= 0.99 of float64 unquantised attention, LSE within 2e-2.
+Cases span several 128-row tiles with ragged tails, both layouts and dtypes, GQA, causal,
+Nq != Nk, head_dim padding (32, 72, 96) and every granularity / accumulation mode.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import attention_fp64, sage_attention, scores as oracle_scores
+from oracle.fp8 import e4m3_encode
+from quantized_attention_mean_gb300.workloads import WORKLOADS, Workload, dense_inputs, to_hnd_f32
+
+from helpers import (TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, cosine, oracle_kw,
+                     out_to_hnd, run_gpu_dense)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    WORKLOADS["tiny"],
+    Workload("ragged_fp16", 1, 2, 2, 300, 300, 64, gran="per_warp", accum="fp32"),
+    Workload("gqa_nhd_bf16", 2, 4, 2, 200, 333, 128, dtype="bf16", layout="NHD", gran="per_thread",
+             accum="fp32", return_lse=True, k_offset_std=3.0),
+    Workload("causal_gqa", 1, 8, 2, 384, 384, 128, dtype="bf16", layout="NHD", is_causal=True,
+             gran="per_thread", accum="fp32", return_lse=True, k_offset_std=3.0),
+    Workload("causal_ragged", 2, 2, 2, 270, 270, 64, is_causal=True, gran="per_block", return_lse=True),
+    Workload("dit_like", 1, 3, 3, 500, 500, 64, dtype="bf16", gran="per_warp", accum="fp16+fp32",
+             smooth_v=True, k_offset_std=4.0, v_offset_std=2.0, return_lse=True),
+    Workload("fp16acc_d128", 1, 2, 2, 512, 512, 128, gran="per_warp", accum="fp16+fp32"),
+    Workload("pad_d32", 1, 2, 2, 130, 130, 32, gran="per_warp", smooth_v=True, return_lse=True),
+    Workload("pad_d72", 1, 2, 1, 140, 260, 72, dtype="bf16", gran="per_thread", accum="fp32+fp32"),
+    Workload("pad_d96", 1, 2, 2, 257, 129, 96, layout="NHD", gran="per_block", is_causal=True),
+    Workload("short_keys", 1, 2, 2, 129, 1, 64, gran="per_warp", smooth_v=True),
+    Workload("q_longer_causal", 1, 2, 2, 300, 100, 64, is_causal=True, gran="per_warp"),
+]
+
+
+def _run(w, seed=0):
+    q, k, v = dense_inputs(w, seed)
+    g = run_gpu_dense(w, q, k, v, debug_scores=True)
+    assert g["status"] == 0
+    qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
+    ref = sage_attention(qn, kn, vn, **oracle_kw(w))
+    return q, k, v, qn, kn, vn, g, ref
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_quantisation_bit_exact(w):
+    import quantized_attention_mean_gb300 as qa
+    _, _, _, qn, kn, vn, g, ref = _run(w)
+    ex = {k: t.cpu().numpy() for k, t in qa.export_quant(g["ws"], w.B, w.Hq, w.Hkv, w.Nq, w.Nk,
+                                                          w.d, w.gran).items()}
+    for b in range(w.B):
+        for h in range(w.Hq):
+            qq = ref["q"][(b, h)]
+            np.testing.assert_array_equal(ex["q8"][b, h], qq["q8"])
+            np.testing.assert_array_equal(ex["sq"][b, h].view(np.uint32), qq["sq"].view(np.uint32))
+        for h in range(w.Hkv):
+            kv = ref["kv"][(b, h)]
+            np.testing.assert_array_equal(ex["kmean"][b, h].view(np.uint32), kv["kbar"].view(np.uint32))
+            np.testing.assert_array_equal(ex["k8"][b, h], kv["k8"])
+            np.testing.assert_array_equal(ex["sk"][b, h].view(np.uint32), kv["sk"].view(np.uint32))
+            np.testing.assert_array_equal(ex["vscale"][b, h].view(np.uint32), kv["sv"].view(np.uint32))
+            if w.smooth_v:
+                np.testing.assert_array_equal(ex["vmean"][b, h].view(np.uint32), kv["vbar"].view(np.uint32))
+            np.testing.assert_array_equal(ex["v8"][b, h], kv["v8"])
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_scores_bit_exact(w):
+    _, _, _, _, _, _, g, ref = _run(w)
+    s = g["scores"].cpu().numpy()
+    grp = w.Hq // w.Hkv
+    for b in range(w.B):
+        for h in range(w.Hq):
+            exact = oracle_scores(ref["q"][(b, h)]["q8"], ref["kv"][(b, h // grp)]["k8"])
+            if w.is_causal:
+                allowed = np.arange(w.Nk)[None, :] <= np.arange(w.Nq)[:, None]
+                np.testing.assert_array_equal(s[b, h][allowed], exact[allowed])
+            else:
+                np.testing.assert_array_equal(s[b, h], exact)
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_output_within_tolerance(w):
+    _, _, _, qn, kn, vn, g, ref = _run(w)
+    o = out_to_hnd(g["out"], w.layout)
+    o_ref = ref["o"]
+    assert np.isfinite(o).all()
+    assert np.abs(o - o_ref).max() <= TOL_MAX_ABS
+    assert cosine(o, o_ref) >= TOL_COS
+    grp = w.Hq // w.Hkv
+    for b in range(w.B):
+        for h in range(w.Hq):
+            of, lf = attention_fp64(qn[b, h], kn[b, h // grp], vn[b, h // grp], ref["sm_scale"], w.is_causal)
+            assert cosine(o[b, h], of) >= TOL_COS_FP64
+    if w.return_lse:
+        lse = g["lse"].cpu().numpy()
+        assert np.abs(lse - ref["lse"]).max() <= TOL_LSE
+
+
+def test_explicit_sm_scale_and_second_seed():
+    w = Workload("scale", 1, 2, 2, 256, 256, 64, gran="per_warp", return_lse=True)
+    q, k, v = dense_inputs(w, seed=5)
+    g = run_gpu_dense(w, q, k, v, sm_scale=0.07)
+    qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
+    ref = sage_attention(qn, kn, vn, **oracle_kw(w, sm_scale=0.07))
+    o = out_to_hnd(g["out"], w.layout)
+    assert np.abs(o - ref["o"]).max() <= TOL_MAX_ABS and cosine(o, ref["o"]) >= TOL_COS
+    assert np.abs(g["lse"].cpu().numpy() - ref["lse"]).max() <= TOL_LSE
+
+
+def test_e4m3_conversion_matches_oracle():
+    import quantized_attention_mean_gb300 as qa
+    rng = np.random.default_rng(0)
+    # every binade around the E4M3 range, each with its rounding ties and neighbours
+    vals = [rng.standard_normal(1 << 20).astype(np.float32) * s for s in (1e-3, 0.1, 1, 30, 400)]
+    ties = []
+    for e in range(-12, 10):
+        for m in range(16):
+            base = np.float32(np.ldexp(1.0 + m / 16.0, e))
+            for dlt in (-1, 0, 1):
+                ties.append(np.nextafter(base, np.float32(np.inf)) if dlt > 0 else
+                            (np.nextafter(base, np.float32(-np.inf)) if dlt < 0 else base))
+    vals.append(np.array(ties, np.float32))
+    vals.append(np.array([0.0, -0.0, 448.0, 449.0, 464.0, 500.0, 1e30, -1e30, 2.0**-9, 2.0**-10, 3 * 2.0**-10], np.float32))
+    x = np.concatenate(vals)
+    x = np.concatenate([x, -x])
+    got = qa.e4m3(torch.from_numpy(x).cuda()).cpu().numpy()
+    np.testing.assert_array_equal(got, e4m3_encode(x))

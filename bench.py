@@ -33,7 +33,7 @@ L2_BYTES = 129 * 2**20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sdpa4k")
@@ -114,7 +114,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -184,7 +184,7 @@ def run_reference(args, w):
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
         return
-    rows = 256
+    rows = 128
     for _ in range(args.warmup):
         oracle_sample(w, rows)
     tot_ops, tot_s = 0.0, 0.0
@@ -317,7 +317,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        rows = 512
+        rows = w.Nq  # one full head
         c_ops, c_s = cpu_baseline_subprocess(w.name, rows)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"batch 0 head 0 of {w.name}: that head's K/V/Q quantisation + {rows} of "

@@ -172,6 +172,12 @@ int sage_attn_debug_scores(const sage_tensor* q, const sage_tensor* k, const sag
                            void* workspace, size_t workspace_bytes, int32_t* scores,
                            void* stream);
 
+/* Test hook: while `on` is non-zero, the attention kernel's producer issues no K/V tile
+ * loads, so the consumers' bounded waits expire (about 2 s) and the device status becomes
+ * SAGE_ERR_TIMEOUT; the kernel still exits cleanly and the context stays usable. Process-wide;
+ * not for concurrent use. Returns SAGE_OK. */
+int sage_debug_stall_attention(int on);
+
 /* Converts n floats (device) to FP8 E4M3 (device bytes) with the round-to-nearest-even,
  * saturating conversion the kernels use for V and P. */
 int sage_debug_e4m3(const float* x, uint8_t* out, int64_t n, void* stream);

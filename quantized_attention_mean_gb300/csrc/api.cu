@@ -103,6 +103,7 @@ void carve(Problem& p, const Layout& L, void* ws) {
 
 // ------------------------------------------------------------------------------ device info
 int g_dev_ok[64];  // 0 unknown, 1 sm_103, 2 other
+int g_stall = 0;   // test hook (sage_debug_stall_attention)
 std::mutex g_mu;
 
 bool device_is_sm103() {
@@ -285,6 +286,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   p.lse = lse;
   p.range_limit = range_limit(nk);
   p.dbg_scores = dbg_scores;
+  p.dbg_stall = g_stall;
   carve(p, L, ws);
   return run_pipeline(p, L, nq, nk, static_cast<cudaStream_t>(stream));
 }
@@ -381,6 +383,7 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
   p.lse = lse;
   p.lse_plane = total_q;
   p.range_limit = 0.f;  // per sequence on the device
+  p.dbg_stall = g_stall;
   carve(p, L, workspace);
   return run_pipeline(p, L, max_seqlen_q, max_seqlen_k, static_cast<cudaStream_t>(stream));
 }
@@ -472,6 +475,11 @@ int sage_profile_read(double* stage_ms, int* calls) {
   }
   *calls = g_prof_used;
   g_prof_used = 0;
+  return SAGE_OK;
+}
+
+int sage_debug_stall_attention(int on) {
+  g_stall = on ? 1 : 0;
   return SAGE_OK;
 }
 

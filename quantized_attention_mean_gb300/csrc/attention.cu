@@ -145,7 +145,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       int issued_k = 0, issued_v = 0;
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
+      if (p.dbg_stall) {
+        // test hook: no K/V tile ever arrives, so every consumer wait runs into its bound
+        volatile int never = 0;
+        mbar_wait(q_full, 0, &never);
+      }
+      for (int j = 0; j < n_tiles && ok && !p.dbg_stall; ++j) {
         const int krow = s.row0_k + j * kTileKeys;
         const int st = j % C::kKStages;
         if (j >= C::kKStages) ok = mbar_wait(&k_empty[st], ((j / C::kKStages) - 1) & 1, abort_flag);

@@ -40,11 +40,12 @@ struct Problem {
   float* kmean; float* vmean; float* vscale;                  // [batch*hkv*d]
   __half* qc; __half* kc; uint8_t* vt;                        // codes
   float* sq; float* sk; float* qkc;                           // scales, LSE correction
-  int* seqinfo;                    // varlen: [5][batch] tok0_q,len_q,row0_q,tok0_k,len_k,row0_k...
+  int* seqinfo;                    // varlen: [kSiRows][batch] per-sequence geometry + LPT order
   int64_t q_rows, k_rows;          // rows per plane in qc / kc (dense: nq / nk)
   int64_t vt_pitch;                // bytes per channel row of vt
   int64_t sq_pp, sk_pp;            // scale groups per plane
   int32_t* dbg_scores;             // optional exact-score dump [B,Hq,Nq,Nk]
+  int dbg_stall;                   // test hook: the producer issues no K/V loads
 };
 
 struct Seq {

@@ -11,6 +11,22 @@ TOL_COS_FP64 = 0.99     # O vs float64 unquantised attention (cosine)
 TOL_LSE = 2e-2          # LSE vs the oracle (absolute)
 
 
+def out_ulp(x, dtype):
+    """One unit in the last place of the output format at |x| (fp16: 11-bit, bf16: 8-bit
+    significand)."""
+    sig, min_exp = (11, -14) if dtype == "fp16" else (8, -126)
+    _, e = np.frexp(np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** min_exp))
+    return np.ldexp(1.0, e - sig)
+
+
+def max_abs_excess(o_gpu, o_ref, dtype):
+    """max(|o_gpu - o_ref| - ulp(o_ref)): the output error beyond the output format's own
+    rounding. The oracle's O is rounded once to the output dtype; two results within the
+    tolerance can round to neighbouring values of that format, so the 2e-2 bound applies on
+    top of one ulp."""
+    return float(np.max(np.abs(np.asarray(o_gpu, np.float64) - o_ref) - out_ulp(o_ref, dtype)))
+
+
 def cosine(a, b):
     a = np.asarray(a, np.float64).ravel()
     b = np.asarray(b, np.float64).ravel()

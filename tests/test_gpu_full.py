@@ -14,7 +14,7 @@ from oracle.attention import attend_head, quantize_kv_head, quantize_q_head, sag
 from quantized_attention_mean_gb300.workloads import (ACC, GRAN, WORKLOADS, dense_inputs, to_hnd_f32,
                                                       varlen_inputs)
 
-from helpers import TOL_COS, TOL_LSE, TOL_MAX_ABS, cosine, out_to_hnd, run_gpu_dense
+from helpers import TOL_COS, TOL_LSE, TOL_MAX_ABS, cosine, max_abs_excess, out_to_hnd, run_gpu_dense
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def test_full_size_dense_sampled(name):
         ref = attend_head(qn[b, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=w.is_causal,
                           accum=ACC[w.accum], rows=rows, qq=qq)
         got = o[b, h, rows]
-        assert np.abs(got - ref["o"]).max() <= TOL_MAX_ABS
+        assert max_abs_excess(got, ref["o"], w.dtype) <= TOL_MAX_ABS
         assert cosine(got, ref["o"]) >= TOL_COS
         if lse is not None:
             assert np.abs(lse[b, h, rows] - ref["lse"]).max() <= TOL_LSE
@@ -84,5 +84,5 @@ def test_full_size_varlen_sampled():
             ref = attend_head(qn[sl, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=False,
                               accum=ACC[w.accum], rows=rows)
             got = o[sl, h][rows]
-            assert np.abs(got - ref["o"]).max() <= TOL_MAX_ABS
+            assert max_abs_excess(got, ref["o"], w.dtype) <= TOL_MAX_ABS
             assert cosine(got, ref["o"]) >= TOL_COS

@@ -20,7 +20,7 @@ const int kQGroup[3] = {128, 32, 1};   // per_block, per_warp, per_thread
 const int kKGroup[3] = {64, 64, 16};
 
 struct Layout {
-  size_t off_err, off_ksum, off_vsum, off_vmin, off_vmax, off_kmean, off_vmean, off_vscale,
+  size_t off_err, off_ksum, off_vsum, off_vmin, off_vmax, off_kmean, off_vmean, off_vscale, off_vrcp,
       off_qc, off_kc, off_vt, off_sq, off_sk, off_qkc, off_seqinfo, total;
   int64_t q_rows, k_rows, vt_pitch, sq_pp, sk_pp, planes_q, planes_kv, n_stats;
   int dp, gq, gk;
@@ -63,6 +63,7 @@ bool make_layout(bool varlen, int batch, int hq, int hkv, int64_t lq, int64_t lk
   L->off_kmean = take(4 * L->n_stats);
   L->off_vmean = take(4 * L->n_stats);
   L->off_vscale = take(4 * L->n_stats);
+  L->off_vrcp = take(4 * L->n_stats);
   L->off_qc = take(2 * (size_t)L->planes_q * L->q_rows * L->dp);
   L->off_kc = take(2 * (size_t)L->planes_kv * L->k_rows * L->dp);
   L->off_vt = take((size_t)L->planes_kv * L->dp * L->vt_pitch);
@@ -84,6 +85,7 @@ void carve(Problem& p, const Layout& L, void* ws) {
   p.kmean = reinterpret_cast<float*>(w + L.off_kmean);
   p.vmean = reinterpret_cast<float*>(w + L.off_vmean);
   p.vscale = reinterpret_cast<float*>(w + L.off_vscale);
+  p.vrcp = reinterpret_cast<float*>(w + L.off_vrcp);
   p.qc = reinterpret_cast<__half*>(w + L.off_qc);
   p.kc = reinterpret_cast<__half*>(w + L.off_kc);
   p.vt = reinterpret_cast<uint8_t*>(w + L.off_vt);
@@ -232,6 +234,7 @@ int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cuda
   if (p.varlen && launch_varlen_setup(p, st) != cudaSuccess) return SAGE_ERR_CUDA;
   if (launch_reset(p, static_cast<int>(L.n_stats), st) != cudaSuccess) return SAGE_ERR_CUDA;
   if (launch_kv_stats(p, max_len_k, st) != cudaSuccess) return SAGE_ERR_CUDA;
+  if (launch_finalize(p, static_cast<int>(L.n_stats), st) != cudaSuccess) return SAGE_ERR_CUDA;
   mark(1);
   if (launch_quant(p, max_len_q > max_len_k ? max_len_q : max_len_k, st) != cudaSuccess)
     return SAGE_ERR_CUDA;

@@ -289,13 +289,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                (p.is_causal && kv0 + kTileKeys - 1 > q_start + x * kTileRows);
         float tile_max = __int_as_float(0xff800000);
         if (!need_mask) {
-          // max of the raw integer scores per sub-group, then scaled (c_g >= 0 keeps order)
+          // max of the raw integer scores per sub-group (three-input max: 8 ops per 16
+          // scores), then scaled (c_g >= 0 keeps the order)
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
-            float mg = __uint_as_float(sr[g >> 1][(g & 1) * 16]);
+            const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
+            float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-            for (int c = 1; c < 16; ++c) mg = fmaxf(mg, __uint_as_float(sr[g >> 1][(g & 1) * 16 + c]));
-            tile_max = fmaxf(tile_max, mg * cg[g]);
+            for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            a = fmaxf(a, __uint_as_float(v[15]));
+            tile_max = fmaxf(tile_max, a * cg[g]);
           }
         } else {
           // masked tile: scale each score; -inf where the key is past the end or causal-masked
@@ -313,20 +316,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
         const float bias = log2_sigma - m_use;
-        // P~ = e4m3(2^(x - m) * sigma), packed 4 per word, and the row sum
+        // P~ = e4m3(2^(x - m) * sigma), packed 4 per word, and the row sum; two scores per
+        // packed fp32 instruction
         uint32_t pk[32];
-        float rs = 0.f;
+        float rs0 = 0.f, rs1 = 0.f;
+        if (!need_mask) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          float e[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float sv = __uint_as_float(sr[(c + u) >> 5][(c + u) & 31]);
-            e[u] = need_mask ? ex2(sv + bias) : ex2(fmaf(sv, cg[(c + u) >> 4], bias));
-            rs += e[u];
+          for (int c = 0; c < 128; c += 4) {
+            float x0, x1, x2, x3;
+            const float cgc = cg[c >> 4];
+            fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
+                 cgc, cgc, bias, bias);
+            fma2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
+                 cgc, cgc, bias, bias);
+            const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+            add2(rs0, rs1, rs0, rs1, e0, e1);
+            add2(rs0, rs1, rs0, rs1, e2, e3);
+            pk[c / 4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
           }
-          pk[c / 4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            float x0, x1, x2, x3;
+            add2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
+                 bias, bias);
+            add2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
+                 bias, bias);
+            const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+            add2(rs0, rs1, rs0, rs1, e0, e1);
+            add2(rs0, rs1, rs0, rs1, e2, e3);
+            pk[c / 4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
+          }
         }
+        const float rs = rs0 + rs1;
         l = l * alpha + rs;
         m = m_new;
         // P tile buffer and O are free once the previous P.V of this tile has completed
@@ -348,7 +370,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tmem_ld32(tO + cc * 32, o);
             tmem_wait_ld(o);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            for (int u = 0; u < 32; u += 2) {
+              float a0, a1;
+              mul2(a0, a1, __uint_as_float(o[u]), __uint_as_float(o[u + 1]), alpha, alpha);
+              o[u] = __float_as_uint(a0);
+              o[u + 1] = __float_as_uint(a1);
+            }
             tmem_st32(tO + cc * 32, o);
           }
           tmem_wait_st();
@@ -387,7 +414,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                   *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
                 }
               } else {
-                for (int u = 0; u < 32 && cc * 32 + u < p.d; ++u) dst[u] = __float2half_rn(v[u]);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                  if (cc * 32 + u < p.d) dst[u] = __float2half_rn(v[u]);
               }
             } else {
               __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + orow + cc * 32;
@@ -400,7 +429,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                   *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
                 }
               } else {
-                for (int u = 0; u < 32 && cc * 32 + u < p.d; ++u) dst[u] = __float2bfloat16_rn(v[u]);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                  if (cc * 32 + u < p.d) dst[u] = __float2bfloat16_rn(v[u]);
               }
             }
           }

@@ -9,7 +9,7 @@ namespace sage {
 
 constexpr int kTileRows = 128;   // query rows per attention tile, tokens per quantisation tile
 constexpr int kTileKeys = 128;   // keys per attention KV tile
-constexpr int kStatsChunk = 512; // tokens per block in the K/V statistics pass
+constexpr int kStatsChunk = 128; // tokens per block in the K/V statistics pass
 
 // Device-side status codes (mirror sage_status in include/sageattn.h).
 enum DevStatus : int { kDevOk = 0, kDevRange = 7, kDevTimeout = 9, kDevSeqlens = 12 };
@@ -37,7 +37,7 @@ struct Problem {
   // workspace
   int* err;
   long long* ksum; long long* vsum; int* vmin; int* vmax;   // [batch*hkv*d]
-  float* kmean; float* vmean; float* vscale;                  // [batch*hkv*d]
+  float* kmean; float* vmean; float* vscale; float* vrcp;     // [batch*hkv*d]
   __half* qc; __half* kc; uint8_t* vt;                        // codes
   float* sq; float* sk; float* qkc;                           // scales, LSE correction
   int* seqinfo;                    // varlen: [kSiRows][batch] per-sequence geometry + LPT order
@@ -94,6 +94,22 @@ __device__ __forceinline__ void load8(const T* row, int c0, int d, int vec16, fl
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = (c0 + i < d) ? to_f32<T>(row[c0 + i]) : 0.0f;
   }
+}
+
+// Raw 16-byte load of channels [c0, c0+8) of one row (channels >= d read as 0).
+template <typename T>
+__device__ __forceinline__ uint4 load8_raw(const T* row, int c0, int d, int vec16) {
+  if (vec16 && c0 + 8 <= d) return __ldg(reinterpret_cast<const uint4*>(row + c0));
+  __align__(16) T h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = (c0 + i < d) ? row[c0 + i] : T(0.0f);
+  return *reinterpret_cast<const uint4*>(h);
+}
+template <typename T>
+__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
+  const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = to_f32<T>(h[i]);
 }
 
 // Two floats -> two E4M3 bytes (RNE, saturate to +-448): byte 0 = lo, byte 1 = hi.

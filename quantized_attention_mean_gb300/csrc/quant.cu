@@ -82,7 +82,7 @@ __global__ void ws_reset_kernel(Problem p, int n_stats) {
 // per (sequence, kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads:
 // thread = (row group rg in 0..15, channel vector vec in 0..15).
 template <typename T>
-__global__ void __launch_bounds__(256) kv_stats_kernel(Problem p) {
+__global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
   const int chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int t0 = chunk * kStatsChunk;
@@ -105,21 +105,30 @@ __global__ void __launch_bounds__(256) kv_stats_kernel(Problem p) {
   const T* kp = static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh;
   const T* vp = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
   if (active) {
-    for (int t = t0 + rg; t < t1; t += 16) {
-      const int64_t tok = (int64_t)(s.tok0_k + t);
-      float vx[8];
-      load8<T>(vp + tok * p.v_sn, c0, p.d, p.vec16, vx);
-      if (p.smooth_k) {
-        float kx[8];
-        load8<T>(kp + tok * p.k_sn, c0, p.d, p.vec16, kx);
+    // every row of this thread (8 rows x K and V) is requested before any is used
+    constexpr int kRows = kStatsChunk / 16;
+    uint4 kr[kRows], vr[kRows];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+    for (int r = 0; r < kRows; ++r) {
+      const int t = t0 + rg + 16 * r;
+      const int64_t tok = (int64_t)(s.tok0_k + t);
+      const bool valid = t < t1;
+      vr[r] = valid ? load8_raw<T>(vp + tok * p.v_sn, c0, p.d, p.vec16) : make_uint4(0, 0, 0, 0);
+      kr[r] = (valid && p.smooth_k) ? load8_raw<T>(kp + tok * p.k_sn, c0, p.d, p.vec16)
+                                    : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      if (t0 + rg + 16 * r >= t1) continue;
+      float vx[8], kx[8];
+      unpack8<T>(vr[r], vx);
+      unpack8<T>(kr[r], kx);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (p.smooth_k) {
           range_bad |= fabsf(kx[i]) >= lim;
           ks[i] += __float2ll_rz(kx[i] * 16777216.0f);
         }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
         if (p.smooth_v) {
           range_bad |= fabsf(vx[i]) >= lim;
           vs[i] += __float2ll_rz(vx[i] * 16777216.0f);
@@ -193,6 +202,29 @@ __global__ void __launch_bounds__(256) kv_stats_kernel(Problem p) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Per (sequence, kv head, channel): the smoothing means from the fixed-point sums, and V's
+// per-channel scale s_v = fl32(absmax/448) and reciprocal fl32(448/absmax), where
+// absmax = max(|fl32(vmax - vmean)|, |fl32(vmin - vmean)|) (x -> fl32(x - m) is monotone, so
+// this equals the max over tokens of |fl32(v - vmean)|). Computed once here so the
+// quantisation pass needs no double-precision arithmetic.
+__global__ void kv_finalize_kernel(Problem p, int n_stats) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_stats) return;
+  const int b = i / (p.hkv * p.d);
+  const Seq s = get_seq(p, b);
+  if (s.len_k <= 0) return;
+  const float km = p.smooth_k ? fixed_point_mean(p.ksum[i], s.len_k) : 0.f;
+  const float vm = p.smooth_v ? fixed_point_mean(p.vsum[i], s.len_k) : 0.f;
+  const float mx = __fsub_rn(ordered_to_float(p.vmax[i]), vm);
+  const float mn = __fsub_rn(ordered_to_float(p.vmin[i]), vm);
+  const float amax = fmaxf(fabsf(mx), fabsf(mn));
+  p.kmean[i] = km;
+  p.vmean[i] = vm;
+  p.vscale[i] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
+  p.vrcp[i] = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+}
+
+// ------------------------------------------------------------------------------------------
 // Quantisation. Grid: (128-token tiles, Hq + 2*Hkv, batch); blockIdx.y selects Q head,
 // K head or V head. 256 threads; thread (rg, vec) holds rows rg + 16*i (i < 8), channels
 // [8*vec, 8*vec + 8).
@@ -222,48 +254,18 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
 
   __shared__ float rowmax[kTileRows];
   __shared__ float grcp[kTileRows];
-  __shared__ __align__(16) uint8_t vtile[128][kTileRows + 16];
+  __shared__ __align__(16) uint8_t vtile[128][kTileRows];
 
-  // per-channel offsets: smoothing means (and for V the scale reciprocal)
-  float mean[8], rcpv[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) { mean[i] = 0.f; rcpv[i] = 0.f; }
-  const bool smooth = kind == 1 ? p.smooth_k : (kind == 2 ? p.smooth_v : false);
-  if (kind != 0 && c0 < d) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + i < d && smooth)
-        mean[i] = fixed_point_mean(kind == 1 ? p.ksum[sidx + c0 + i] : p.vsum[sidx + c0 + i],
-                                   s.len_k);
-  }
-  float kmean_q[8];   // for the Q-side LSE term
-#pragma unroll
-  for (int i = 0; i < 8; ++i) kmean_q[i] = 0.f;
+  // per-channel values from the finalize pass: smoothing means, V scale reciprocals, and for
+  // Q heads the K mean used by the LSE term
+  float mean[8], rcpv[8], kmean_q[8];
   const bool want_qkc = kind == 0 && p.return_lse && p.smooth_k;
-  if (want_qkc && c0 < d) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + i < d) kmean_q[i] = fixed_point_mean(p.ksum[sidx + c0 + i], s.len_k);
-  }
-  if (kind == 2 && c0 < d) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (c0 + i < d) {
-        const float mx = __fsub_rn(ordered_to_float(p.vmax[sidx + c0 + i]), mean[i]);
-        const float mn = __fsub_rn(ordered_to_float(p.vmin[sidx + c0 + i]), mean[i]);
-        const float amax = fmaxf(fabsf(mx), fabsf(mn));
-        rcpv[i] = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
-        if (tile == 0) {
-          p.vscale[sidx + c0 + i] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
-          p.vmean[sidx + c0 + i] = mean[i];
-        }
-      }
-    }
-  }
-  if (kind == 1 && tile == 0 && c0 < d) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + i < d) p.kmean[sidx + c0 + i] = mean[i];
+  for (int i = 0; i < 8; ++i) {
+    const bool ch = c0 + i < d;
+    mean[i] = (ch && kind == 1) ? p.kmean[sidx + c0 + i] : ((ch && kind == 2) ? p.vmean[sidx + c0 + i] : 0.f);
+    rcpv[i] = (ch && kind == 2) ? p.vrcp[sidx + c0 + i] : 0.f;
+    kmean_q[i] = (ch && want_qkc) ? p.kmean[sidx + c0 + i] : 0.f;
   }
 
   // load the tile (values past the sequence end and channels past d are 0), smoothed
@@ -300,8 +302,9 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
       for (int j = 0; j < 8; j += 2) {
         const uint32_t two = pack_e4m3x2(__fmul_rn(x[i][j], rcpv[j]), __fmul_rn(x[i][j + 1], rcpv[j + 1]));
         if (c0 + j < dp) {
-          vtile[c0 + j][rr] = static_cast<uint8_t>(two & 0xFF);
-          vtile[c0 + j + 1][rr] = static_cast<uint8_t>(two >> 8);
+          const int sw = (vec & 7) << 4;  // 16-byte chunk swizzle per channel octet
+          vtile[c0 + j][rr ^ sw] = static_cast<uint8_t>(two & 0xFF);
+          vtile[c0 + j + 1][rr ^ sw] = static_cast<uint8_t>(two >> 8);
         }
       }
     }
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     for (int idx = threadIdx.x; idx < dp * 8; idx += 256) {
       const int c = idx >> 3, ch = (idx & 7) * 16;
       if (ch < ncols) {
-        uint4 val = *reinterpret_cast<const uint4*>(&vtile[c][ch]);
+        uint4 val = *reinterpret_cast<const uint4*>(&vtile[c][ch ^ (((c >> 3) & 7) << 4)]);
         *reinterpret_cast<uint4*>(p.vt + (plane * dp + c) * p.vt_pitch + col0 + ch) = val;
       }
     }
@@ -335,18 +338,36 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     if (vec == 0) rowmax[rg + 16 * i] = a;
   }
   __syncthreads();
-  const int ngroups = kTileRows / gs;
   const int64_t plane = plane_of(p, b, h, kind == 0 ? p.hq : p.hkv);
   const int row0 = kind == 0 ? s.row0_q : s.row0_k;
-  if (threadIdx.x < ngroups) {
-    const int g = threadIdx.x;
+  {
+    // group absmax: warps 0-3 each own 32 consecutive rows; groups of <= 32 rows reduce with
+    // shuffles, groups of 64 / 128 rows combine the per-warp maxima
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float wmax[4];
     float a = 0.f;
-    for (int r = g * gs; r < (g + 1) * gs; ++r) a = fmaxf(a, rowmax[r]);
-    grcp[g] = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
-    if (r0 + g * gs < len) {
-      float* sc = kind == 0 ? p.sq : p.sk;
-      const int64_t pp = kind == 0 ? p.sq_pp : p.sk_pp;
-      sc[plane * pp + (row0 + r0) / gs + g] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+    if (warp < 4) {
+      a = rowmax[warp * 32 + lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1)
+        if (off < gs) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+      if (lane == 0) wmax[warp] = a;
+    }
+    __syncthreads();
+    if (warp < 4 && gs > 32) {
+      const int w0 = (warp * 32 / gs) * (gs / 32);
+      a = wmax[w0];
+      for (int w = 1; w < gs / 32; ++w) a = fmaxf(a, wmax[w0 + w]);
+    }
+    const int r = warp * 32 + lane;  // row of this lane (warps 0-3)
+    if (warp < 4 && r % gs == 0) {
+      const int g = r / gs;
+      grcp[g] = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
+      if (r0 + r < len) {
+        float* sc = kind == 0 ? p.sq : p.sk;
+        const int64_t pp = kind == 0 ? p.sq_pp : p.sk_pp;
+        sc[plane * pp + (row0 + r0) / gs + g] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -425,6 +446,11 @@ cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
   const dim3 grid((max_len_k + kStatsChunk - 1) / kStatsChunk, p.hkv, p.batch);
   if (p.dtype == 0) kv_stats_kernel<__half><<<grid, 256, 0, st>>>(p);
   else kv_stats_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st) {
+  kv_finalize_kernel<<<(n_stats + 255) / 256, 256, 0, st>>>(p, n_stats);
   return cudaGetLastError();
 }
 

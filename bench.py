@@ -335,7 +335,7 @@ def run_ours(args, w):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 7 * args.steps,  # reset, stats, finalize, quant Q/K/V, attention
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -236,8 +236,7 @@ int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cuda
   if (launch_kv_stats(p, max_len_k, st) != cudaSuccess) return SAGE_ERR_CUDA;
   if (launch_finalize(p, static_cast<int>(L.n_stats), st) != cudaSuccess) return SAGE_ERR_CUDA;
   mark(1);
-  if (launch_quant(p, max_len_q > max_len_k ? max_len_q : max_len_k, st) != cudaSuccess)
-    return SAGE_ERR_CUDA;
+  if (launch_quant(p, max_len_q, max_len_k, st) != cudaSuccess) return SAGE_ERR_CUDA;
   mark(2);
   const int pairs = (max_len_q + 2 * kTileRows - 1) / (2 * kTileRows);
   if (launch_attention(p, maps, pairs, st) != cudaSuccess) return SAGE_ERR_CUDA;

@@ -43,7 +43,7 @@ struct AttnCfg {
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 1;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
@@ -62,7 +62,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 template <int DP>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __maxnreg__(200)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Problem p) {
   using C = AttnCfg<DP>;
@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* s_full = v_empty + C::kVStages;  // [2]
   uint64_t* p_full = s_full + 2;             // [2]
   uint64_t* o_full = p_full + 2;             // [2]
-  uint64_t* drain = o_full + 2;
+  uint64_t* o_ready = o_full + 2;            // [2]
+  uint64_t* drain = o_ready + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
 
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
+      mbar_init(&o_ready[i], 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sv = j % C::kVStages;
         const int nst = (j + 1) % C::kKStages;
         for (int x = 0; x < nx && ok; ++x) {
+          // S_j(x) consumed and P_j(x) written: the tile's next scores can start right away
           ok = mbar_wait(&p_full[x], j & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -220,6 +223,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             issue_qk(x, nst);
           }
+          // O(x) rescaled for the new running max: accumulate P_j(x) V_j
+          ok = mbar_wait(&o_ready[x], j & 1, abort_flag);
+          if (!ok) break;
           if (x == 0) ok = mbar_wait(&v_full[sv], (j / C::kVStages) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -256,6 +262,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float m = __int_as_float(0xff800000);  // running max (log2 units)
     float l = 0.f;                          // running sum of 2^(x - m) * sigma
     bool ok = true;
+    // K scales of the 8 sub-groups of 16 keys, loaded one tile ahead of their use
+    float skn[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) skn[g] = g * 16 < s.len_k ? __ldg(&skp[(g * 16) / gk]) : 0.f;
     if (active_tile) {
       for (int j = 0; j < n_tiles; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
@@ -281,9 +291,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // (a K scale group is 16 or 64 keys, so each sub-group has one scale)
         float cg[8];
 #pragma unroll
+        for (int g = 0; g < 8; ++g) cg[g] = row_scale * skn[g];
+#pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const int kg = kv0 + g * 16;
-          cg[g] = kg < s.len_k ? row_scale * __ldg(&skp[kg / gk]) : 0.f;
+          const int kg = kv0 + kTileKeys + g * 16;
+          skn[g] = kg < s.len_k ? __ldg(&skp[kg / gk]) : 0.f;
         }
         const bool need_mask = (kv0 + kTileKeys > s.len_k) ||
                                (p.is_causal && kv0 + kTileKeys - 1 > q_start + x * kTileRows);
@@ -319,36 +331,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // P~ = e4m3(2^(x - m) * sigma), packed 4 per word, and the row sum; two scores per
         // packed fp32 instruction
         uint32_t pk[32];
-        float rs0 = 0.f, rs1 = 0.f;
-        if (!need_mask) {
+        float gsum[16];  // a pair of partial row sums per 16-key sub-group
 #pragma unroll
-          for (int c = 0; c < 128; c += 4) {
+        for (int g = 0; g < 8; ++g) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int c = g * 16; c < g * 16 + 16; c += 4) {
             float x0, x1, x2, x3;
-            const float cgc = cg[c >> 4];
-            fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
-                 cgc, cgc, bias, bias);
-            fma2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
-                 cgc, cgc, bias, bias);
+            const float s0 = __uint_as_float(sr[c >> 5][c & 31]);
+            const float s1 = __uint_as_float(sr[c >> 5][(c & 31) + 1]);
+            const float s2 = __uint_as_float(sr[c >> 5][(c & 31) + 2]);
+            const float s3 = __uint_as_float(sr[c >> 5][(c & 31) + 3]);
+            if (!need_mask) {
+              fma2(x0, x1, s0, s1, cg[g], cg[g], bias, bias);
+              fma2(x2, x3, s2, s3, cg[g], cg[g], bias, bias);
+            } else {
+              add2(x0, x1, s0, s1, bias, bias);
+              add2(x2, x3, s2, s3, bias, bias);
+            }
             const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
-            add2(rs0, rs1, rs0, rs1, e0, e1);
-            add2(rs0, rs1, rs0, rs1, e2, e3);
+            add2(a0, a1, a0, a1, e0, e1);
+            add2(a0, a1, a0, a1, e2, e3);
             pk[c / 4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; c += 4) {
-            float x0, x1, x2, x3;
-            add2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
-                 bias, bias);
-            add2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
-                 bias, bias);
-            const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
-            add2(rs0, rs1, rs0, rs1, e0, e1);
-            add2(rs0, rs1, rs0, rs1, e2, e3);
-            pk[c / 4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
-          }
+          gsum[2 * g] = a0;
+          gsum[2 * g + 1] = a1;
         }
-        const float rs = rs0 + rs1;
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int u = 0; u < w; ++u) gsum[u] += gsum[u + w];
+        const float rs = gsum[0];
         l = l * alpha + rs;
         m = m_new;
         // P tile buffer and O are free once the previous P.V of this tile has completed
@@ -363,25 +376,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           *reinterpret_cast<uint4*>(my_p + ((ch ^ (r & 7)) << 4)) = val;
         }
         fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+        // rescale this warp's O rows for the grown max while the next scores are computed;
+        // P_j(x) V_j is issued only after o_ready
         if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
+          uint32_t o[DP / 32][32];
+#pragma unroll
+          for (int cc = 0; cc < DP / 32; ++cc) tmem_ld32(tO + cc * 32, o[cc]);
+#pragma unroll
+          for (int cc = 0; cc < DP / 32; ++cc) tmem_wait_ld(o[cc]);
 #pragma unroll
           for (int cc = 0; cc < DP / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tO + cc * 32, o);
-            tmem_wait_ld(o);
 #pragma unroll
             for (int u = 0; u < 32; u += 2) {
               float a0, a1;
-              mul2(a0, a1, __uint_as_float(o[u]), __uint_as_float(o[u + 1]), alpha, alpha);
-              o[u] = __float_as_uint(a0);
-              o[u + 1] = __float_as_uint(a1);
+              mul2(a0, a1, __uint_as_float(o[cc][u]), __uint_as_float(o[cc][u + 1]), alpha, alpha);
+              o[cc][u] = __float_as_uint(a0);
+              o[cc][u + 1] = __float_as_uint(a1);
             }
-            tmem_st32(tO + cc * 32, o);
+            tmem_st32(tO + cc * 32, o[cc]);
           }
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&p_full[x]);
+        mbar_arrive(&o_ready[x]);
       }
       // ---- epilogue
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (n_tiles - 1) & 1, abort_flag));

@@ -9,7 +9,7 @@ cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st);
 cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st);
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st);
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st);
-cudaError_t launch_quant(const Problem& p, int max_len, cudaStream_t st);
+cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st);
 cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, int d, int planes,
                                 int n, int8_t* out, cudaStream_t st);
 cudaError_t launch_export_vt(const uint8_t* vt, int64_t pitch, int dp, int d, int planes, int n,

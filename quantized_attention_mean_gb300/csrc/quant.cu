@@ -225,8 +225,8 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Quantisation. Grid: (128-token tiles, Hq + 2*Hkv, batch); blockIdx.y selects Q head,
-// K head or V head. 256 threads; thread (rg, vec) holds rows rg + 16*i (i < 8), channels
+// Quantisation, one instantiation per tensor (kind 0 = Q, 1 = K, 2 = V). Grid: (128-token
+// tiles, heads, batch). 256 threads; thread (rg, vec) holds rows rg + 16*i (i < 8), channels
 // [8*vec, 8*vec + 8).
 //   Q: codes = INT8 per group of gq rows (stored as integer-valued fp16 for the tensor
 //      cores), scales sq, and (return_lse with smooth_k) the LSE term q . kmean.
@@ -234,11 +234,9 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //   V: V' = V - vmean, E4M3 with the per-channel scale absmax/448, written transposed
 //      [channel][token] so that P.V reads V^T tiles K-major.
 // Rows past the sequence end up to the stored tile end are written as zeros.
-template <typename T>
-__global__ void __launch_bounds__(256) quant_kernel(Problem p) {
-  const int tile = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
-  const int kind = y < p.hq ? 0 : (y < p.hq + p.hkv ? 1 : 2);
-  const int h = kind == 0 ? y : (kind == 1 ? y - p.hq : y - p.hq - p.hkv);
+template <typename T, int kind>
+__global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
+  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int len = kind == 0 ? s.len_q : s.len_k;
   // rows stored for this sequence: dense planes hold exactly len rows; varlen segments are
@@ -249,7 +247,7 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
   const int vec = threadIdx.x & 15, rg = threadIdx.x >> 4;
   const int c0 = vec * 8;
   const int d = p.d, dp = p.dp;
-  const int hk = kind == 0 ? y / (p.hq / p.hkv) : h;   // kv head feeding this q head
+  const int hk = kind == 0 ? h / (p.hq / p.hkv) : h;   // kv head feeding this q head
   const int64_t sidx = ((int64_t)b * p.hkv + hk) * d;
 
   __shared__ float rowmax[kTileRows];
@@ -268,7 +266,8 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     kmean_q[i] = (ch && want_qkc) ? p.kmean[sidx + c0 + i] : 0.f;
   }
 
-  // load the tile (values past the sequence end and channels past d are 0), smoothed
+  // load the tile as raw 16-byte words (values past the sequence end and channels past d are
+  // 0); every row of the thread is requested before any is used
   const T* base;
   int64_t sn;
   if (kind == 0) {
@@ -279,28 +278,31 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     base = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)h * p.v_sh; sn = p.v_sn;
   }
   const int tok0 = kind == 0 ? s.tok0_q : s.tok0_k;
-  float x[8][8];
+  uint4 raw[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = r0 + rg + 16 * i;
-    if (r < len && c0 < d) {
-      load8<T>(base + (int64_t)(tok0 + r) * sn, c0, d, p.vec16, x[i]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[i][j] = (c0 + j < d) ? __fsub_rn(x[i][j], mean[j]) : 0.f;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
-    }
+    raw[i] = (r < len && c0 < d) ? load8_raw<T>(base + (int64_t)(tok0 + r) * sn, c0, d, p.vec16)
+                                 : make_uint4(0, 0, 0, 0);
   }
+  // smoothed fp32 values of row i (x - mean, one IEEE subtraction; 0 past the end / past d)
+  auto row_values = [&](int i, float (&x)[8]) {
+    unpack8<T>(raw[i], x);
+    const bool live = r0 + rg + 16 * i < len;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = (live && c0 + j < d) ? __fsub_rn(x[j], mean[j]) : 0.f;
+  };
 
   if (kind == 2) {
     // ---- V: E4M3 codes, transposed through shared memory
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int rr = rg + 16 * i;
+      float x[8];
+      row_values(i, x);
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        const uint32_t two = pack_e4m3x2(__fmul_rn(x[i][j], rcpv[j]), __fmul_rn(x[i][j + 1], rcpv[j + 1]));
+        const uint32_t two = pack_e4m3x2(__fmul_rn(x[j], rcpv[j]), __fmul_rn(x[j + 1], rcpv[j + 1]));
         if (c0 + j < dp) {
           const int sw = (vec & 7) << 4;  // 16-byte chunk swizzle per channel octet
           vtile[c0 + j][rr ^ sw] = static_cast<uint8_t>(two & 0xFF);
@@ -328,9 +330,11 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
   const int gs = kind == 0 ? p.gq : p.gk;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
+    float x[8];
+    row_values(i, x);
     float a = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[i][j]));
+    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
@@ -378,10 +382,12 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     const int rr = rg + 16 * i;
     const int r = r0 + rr;
     const float rc = grcp[rr / gs];
+    float x[8];
+    row_values(i, x);
     __align__(16) __half hv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      int c = __float2int_rn(__fmul_rn(x[i][j], rc));
+      int c = __float2int_rn(__fmul_rn(x[j], rc));
       c = max(-127, min(127, c));
       hv[j] = __int2half_rn(c);
     }
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(256) quant_kernel(Problem p) {
     if (want_qkc) {
       float dot = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) dot = fmaf(x[i][j], kmean_q[j], dot);
+      for (int j = 0; j < 8; ++j) dot = fmaf(x[j], kmean_q[j], dot);
       dot += __shfl_xor_sync(0xffffffffu, dot, 1);
       dot += __shfl_xor_sync(0xffffffffu, dot, 2);
       dot += __shfl_xor_sync(0xffffffffu, dot, 4);
@@ -454,10 +460,18 @@ cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant(const Problem& p, int max_len, cudaStream_t st) {
-  const dim3 grid((max_len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
-  if (p.dtype == 0) quant_kernel<__half><<<grid, 256, 0, st>>>(p);
-  else quant_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+template <typename T>
+static void launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
+  const dim3 gq((max_len_q + kTileRows - 1) / kTileRows, p.hq, p.batch);
+  const dim3 gk((max_len_k + kTileRows - 1) / kTileRows, p.hkv, p.batch);
+  quant_kernel<T, 0><<<gq, 256, 0, st>>>(p);
+  quant_kernel<T, 1><<<gk, 256, 0, st>>>(p);
+  quant_kernel<T, 2><<<gk, 256, 0, st>>>(p);
+}
+
+cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
+  if (p.dtype == 0) launch_quant_t<__half>(p, max_len_q, max_len_k, st);
+  else launch_quant_t<__nv_bfloat16>(p, max_len_q, max_len_k, st);
   return cudaGetLastError();
 }
 

@@ -132,6 +132,10 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
 /* Human-readable name of a sage_status. Never NULL. */
 const char* sage_status_string(int status);
 
+/* Name and description of the CUDA error behind the calling thread's most recent
+ * SAGE_ERR_CUDA ("no error" if there was none). Never NULL. */
+const char* sage_last_cuda_error(void);
+
 /* Synchronises `stream`, then returns the status the device recorded in `workspace`
  * during the last call that used it (SAGE_OK if none), or SAGE_ERR_CUDA. */
 int sage_read_device_status(const void* workspace, void* stream);

@@ -28,7 +28,10 @@ DTYPE = {torch.float16: 0, torch.bfloat16: 1}
 class SageError(RuntimeError):
     def __init__(self, status, what=""):
         self.status = status
-        msg = _lib.load().sage_status_string(status).decode()
+        lib = _lib.load()
+        msg = lib.sage_status_string(status).decode()
+        if status == 10:  # SAGE_ERR_CUDA: name the failing call
+            msg += " [" + lib.sage_last_cuda_error().decode() + "]"
         super().__init__(f"{what}: {msg}" if what else msg)
 
 

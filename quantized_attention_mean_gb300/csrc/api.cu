@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/sageattn.h: argument validation, workspace
 // carving, TMA tensor maps and the launch sequence. No device memory is allocated here.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -216,6 +217,15 @@ StageEvents* prof_next() {
   return &g_prof_pool[g_prof_used++];
 }
 
+thread_local char g_last_err[192] = "no error";
+
+// Records a failed CUDA call for sage_last_cuda_error and returns SAGE_ERR_CUDA.
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_err, sizeof(g_last_err), "%s: %s (%s)", where, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return SAGE_ERR_CUDA;
+}
+
 int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cudaStream_t st) {
   CUtensorMap maps[3];
   const uint64_t dp = static_cast<uint64_t>(L.dp);
@@ -226,20 +236,21 @@ int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cuda
             make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.vt,
                      p.varlen ? L.k_rows : static_cast<uint64_t>(p.nk), dp, L.planes_kv,
                      L.vt_pitch, L.vt_pitch * dp, 128, L.dp);
-  if (!ok) return SAGE_ERR_CUDA;
+  if (!ok) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   StageEvents* ev = prof_next();
   auto mark = [&](int i) { if (ev) cudaEventRecord(ev->e[i], st); };
+  cudaError_t e;
   mark(0);
-  if (cudaMemsetAsync(p.err, 0, 4, st) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (p.varlen && launch_varlen_setup(p, st) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (launch_reset(p, static_cast<int>(L.n_stats), st) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (launch_kv_stats(p, max_len_k, st) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (launch_finalize(p, static_cast<int>(L.n_stats), st) != cudaSuccess) return SAGE_ERR_CUDA;
+  if ((e = cudaMemsetAsync(p.err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "status reset");
+  if (p.varlen && (e = launch_varlen_setup(p, st)) != cudaSuccess) return cuda_fail(e, "varlen set-up");
+  if ((e = launch_reset(p, static_cast<int>(L.n_stats), st)) != cudaSuccess) return cuda_fail(e, "statistics reset");
+  if ((e = launch_kv_stats(p, max_len_k, st)) != cudaSuccess) return cuda_fail(e, "K/V statistics");
+  if ((e = launch_finalize(p, static_cast<int>(L.n_stats), st)) != cudaSuccess) return cuda_fail(e, "statistics finalize");
   mark(1);
-  if (launch_quant(p, max_len_q, max_len_k, st) != cudaSuccess) return SAGE_ERR_CUDA;
+  if ((e = launch_quant(p, max_len_q, max_len_k, st)) != cudaSuccess) return cuda_fail(e, "quantisation");
   mark(2);
   const int pairs = (max_len_q + 2 * kTileRows - 1) / (2 * kTileRows);
-  if (launch_attention(p, maps, pairs, st) != cudaSuccess) return SAGE_ERR_CUDA;
+  if ((e = launch_attention(p, maps, pairs, st)) != cudaSuccess) return cuda_fail(e, "attention");
   mark(3);
   return SAGE_OK;
 }
@@ -408,6 +419,8 @@ const char* sage_status_string(int status) {
     default: return "unknown sage_status";
   }
 }
+
+const char* sage_last_cuda_error(void) { return g_last_err; }
 
 int sage_read_device_status(const void* workspace, void* stream) {
   if (!workspace) return SAGE_ERR_INVALID_ARG;

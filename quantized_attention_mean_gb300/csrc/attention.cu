@@ -26,7 +26,12 @@
 
 namespace sage {
 
-constexpr int kAttnThreads = 320;  // 10 warps
+// 12 warps = 3 warpgroups: softmax A (warps 0-3), softmax B (4-7), and a control warpgroup
+// (warp 8 TMA, warp 9 MMA + TMEM allocation, warps 10-11 idle). Launched at 168 registers
+// per thread (the per-sub-partition limit with 3 warps each); the control warpgroup drops to
+// 56 and the softmax warpgroups rise to 224: 2*128*224 + 128*56 = 12*32*168.
+constexpr int kAttnThreads = 384;
+constexpr uint32_t kRegsSoftmax = 224, kRegsControl = 56;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DP>
@@ -62,7 +67,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 template <int DP>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Problem p) {
   using C = AttnCfg<DP>;
@@ -131,7 +136,9 @@ __global__ void __maxnreg__(200)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp >= 8) {
+   regs_dec<kRegsControl>();
+   if (warp == 8) {
     // =========================================================== TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -180,7 +187,7 @@ __global__ void __maxnreg__(200)
         record_error(p.err, kDevTimeout);
       }
     }
-  } else if (warp == 9) {
+   } else if (warp == 9) {
     // =========================================================== MMA issuer
     if (lane == 0) {
       const uint32_t sq_addr = smem_u32(sQ), sk_addr = smem_u32(sK), sv_addr = smem_u32(sV),
@@ -241,7 +248,9 @@ __global__ void __maxnreg__(200)
       mbar_wait(drain, 0, &never);
       if (!ok) record_error(p.err, kDevTimeout);
     }
+   }
   } else {
+    regs_inc<kRegsSoftmax>();
     // =========================================================== softmax (warps 0-7)
     const int x = warp >> 2;               // tile A or B
     const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane

@@ -184,6 +184,18 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- register reallocation
+// Warpgroup-wide (all 4 warps execute it): lower / raise this warpgroup's per-thread
+// register budget. The raises of a block must fit in what its lowers release.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- packed fp32 ALU
 // Two-lane fp32 arithmetic (one instruction for two IEEE-rounded results) and the
 // three-input max: they halve the issue cost of the per-score softmax math.

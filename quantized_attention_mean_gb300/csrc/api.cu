@@ -102,11 +102,13 @@ void carve(Problem& p, const Layout& L, void* ws) {
   p.dp = L.dp;
   p.gq = L.gq;
   p.gk = L.gk;
+  p.lgk = L.gk == 16 ? 4 : 6;
 }
 
 // ------------------------------------------------------------------------------ device info
 int g_dev_ok[64];  // 0 unknown, 1 sm_103, 2 other
 int g_stall = 0;   // test hook (sage_debug_stall_attention)
+long long* g_trace = nullptr;  // sage_debug_trace_attention
 std::mutex g_mu;
 
 bool device_is_sm103() {
@@ -300,6 +302,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   p.range_limit = range_limit(nk);
   p.dbg_scores = dbg_scores;
   p.dbg_stall = g_stall;
+  p.dbg_trace = g_trace;
   carve(p, L, ws);
   return run_pipeline(p, L, nq, nk, static_cast<cudaStream_t>(stream));
 }
@@ -490,6 +493,11 @@ int sage_profile_read(double* stage_ms, int* calls) {
   }
   *calls = g_prof_used;
   g_prof_used = 0;
+  return SAGE_OK;
+}
+
+int sage_debug_trace_attention(long long* clocks) {
+  g_trace = clocks;
   return SAGE_OK;
 }
 

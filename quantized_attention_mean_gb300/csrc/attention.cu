@@ -66,6 +66,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// a[idx] for a runtime idx in [0, 8) without indexing a register array.
+__device__ __forceinline__ float pick8(const float (&a)[8], int idx) {
+  float v = a[0];
+#pragma unroll
+  for (int g = 1; g < 8; ++g) v = idx == g ? a[g] : v;
+  return v;
+}
+
+// Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0).
+__device__ __forceinline__ void trace(const Problem& p, bool on, int role, int tile, int ev) {
+  if (on && tile < kTraceTiles)
+    p.dbg_trace[(role * kTraceTiles + tile) * kTraceEvents + ev] = clock64();
+}
+
 template <int DP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -93,6 +107,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tr = p.dbg_trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   // ---- work item: (query head, 256-row pair, sequence); heaviest pairs first when causal
   const int h = blockIdx.x;
@@ -164,6 +179,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int st = j % C::kKStages;
         if (j >= C::kKStages) ok = mbar_wait(&k_empty[st], ((j / C::kKStages) - 1) & 1, abort_flag);
         if (!ok) break;
+        trace(p, tr, 3, j, 0);
         mbar_arrive_expect_tx(&k_full[st], C::kKTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sK + st * C::kKTileBytes + c * kTileKeys * 128, &tmK, &k_full[st], c * 64,
@@ -172,6 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sv = j % C::kVStages;
         if (j >= C::kVStages) ok = mbar_wait(&v_empty[sv], ((j / C::kVStages) - 1) & 1, abort_flag);
         if (!ok) break;
+        trace(p, tr, 3, j, 1);
         mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
         tma_load_3d(sV + sv * C::kVTileBytes, &tmV, &v_full[sv], krow, 0, (int)plane_kv);
         ++issued_v;
@@ -223,6 +240,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // S_j(x) consumed and P_j(x) written: the tile's next scores can start right away
           ok = mbar_wait(&p_full[x], j & 1, abort_flag);
           if (!ok) break;
+          trace(p, tr, 2, j, 4 * x + 0);
           tc_fence_after();
           if (j + 1 < n_tiles) {
             if (x == 0) ok = mbar_wait(&k_full[nst], ((j + 1) / C::kKStages) & 1, abort_flag);
@@ -230,13 +248,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             issue_qk(x, nst);
           }
+          trace(p, tr, 2, j, 4 * x + 1);
           // O(x) rescaled for the new running max: accumulate P_j(x) V_j
           ok = mbar_wait(&o_ready[x], j & 1, abort_flag);
           if (!ok) break;
+          trace(p, tr, 2, j, 4 * x + 2);
           if (x == 0) ok = mbar_wait(&v_full[sv], (j / C::kVStages) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_pv(x, sv, j == 0);
+          trace(p, tr, 2, j, 4 * x + 3);
         }
         if (!ok) break;
         if (j + 1 < n_tiles) mma_commit(&k_empty[nst]);
@@ -263,55 +284,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int i = q_start + x * kTileRows + r;  // query row within the sequence
     const bool row_valid = active_tile && r < xrows;
     const float log2_sigma = p.acc_mode == 1 ? 0.0f : 8.807354922057604f;  // log2(448)
+    const bool trs = tr && (warp & 3) == 0 && lane == 0;
     float sq = 0.f;
     if (row_valid) sq = __ldg(&p.sq[plane_q * p.sq_pp + (s.row0_q + i) / p.gq]);
     const float row_scale = sq * p.sm_scale * kLog2e;
-    const float* skp = p.sk + plane_kv * p.sk_pp + s.row0_k / p.gk;
-    const int gk = p.gk;
+    const float* skp = p.sk + plane_kv * p.sk_pp + (s.row0_k >> p.lgk);
+    const int lgk = p.lgk;  // log2 of the K scale group (16 or 64 keys)
     float m = __int_as_float(0xff800000);  // running max (log2 units)
     float l = 0.f;                          // running sum of 2^(x - m) * sigma
     bool ok = true;
     // K scales of the 8 sub-groups of 16 keys, loaded one tile ahead of their use
     float skn[8];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) skn[g] = g * 16 < s.len_k ? __ldg(&skp[(g * 16) / gk]) : 0.f;
+    for (int g = 0; g < 8; ++g) skn[g] = g * 16 < s.len_k ? __ldg(&skp[(g * 16) >> lgk]) : 0.f;
+    // keys this row may see: [0, row_limit) (causal: j <= i; always: j < len_k)
+    const int row_limit = p.is_causal ? min(s.len_k, i + 1) : s.len_k;
     if (active_tile) {
       for (int j = 0; j < n_tiles; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
         if (!ok) break;
+        trace(p, trs, x, j, 0);
         tc_fence_after();
-        uint32_t sr[4][32];
-        tmem_ld32(tS + 0, sr[0]);
-        tmem_ld32(tS + 32, sr[1]);
-        tmem_ld32(tS + 64, sr[2]);
-        tmem_ld32(tS + 96, sr[3]);
-        tmem_wait_ld(sr[0]);
-        tmem_wait_ld(sr[1]);
-        tmem_wait_ld(sr[2]);
-        tmem_wait_ld(sr[3]);
         const int kv0 = j * kTileKeys;
-        if (p.dbg_scores != nullptr && row_valid) {
-          int32_t* dst = p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk;
+        const int limit = row_limit - kv0;  // this row's allowed keys in the tile: [0, limit)
+        const bool masked = __any_sync(0xffffffffu, limit < kTileKeys);
+        if (p.dbg_scores != nullptr) {
+          // test hook: the integer scores as read from tensor memory
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t t[32];
+            tmem_ld32(tS + ch * 32, t);
+            tmem_wait_ld(t);
+            if (row_valid) {
+              int32_t* dst = p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk + kv0 + ch * 32;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (kv0 + c < s.len_k) dst[kv0 + c] = __float2int_rn(__uint_as_float(sr[c >> 5][c & 31]));
+              for (int u = 0; u < 32; ++u)
+                if (kv0 + ch * 32 + u < s.len_k) dst[u] = __float2int_rn(__uint_as_float(t[u]));
+            }
+          }
         }
         // multipliers c_g = s_q * s_k * sm_scale * log2(e) for the 8 sub-groups of 16 keys
         // (a K scale group is 16 or 64 keys, so each sub-group has one scale)
         float cg[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) cg[g] = row_scale * skn[g];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int kg = kv0 + kTileKeys + g * 16;
-          skn[g] = kg < s.len_k ? __ldg(&skp[kg / gk]) : 0.f;
-        }
-        const bool need_mask = (kv0 + kTileKeys > s.len_k) ||
-                               (p.is_causal && kv0 + kTileKeys - 1 > q_start + x * kTileRows);
+        uint32_t sr[4][32];
         float tile_max = __int_as_float(0xff800000);
-        if (!need_mask) {
-          // max of the raw integer scores per sub-group (three-input max: 8 ops per 16
-          // scores), then scaled (c_g >= 0 keeps the order)
+        if (!masked) {
+          // every key of the tile is visible: scores stay in registers
+          tmem_ld32(tS + 0, sr[0]);
+          tmem_ld32(tS + 32, sr[1]);
+          tmem_ld32(tS + 64, sr[2]);
+          tmem_ld32(tS + 96, sr[3]);
+          tmem_wait_ld(sr[0]);
+          tmem_wait_ld(sr[1]);
+          tmem_wait_ld(sr[2]);
+          tmem_wait_ld(sr[3]);
+          trace(p, trs, x, j, 1);
+          // max of the raw integer scores per sub-group (three-input max), then scaled
+          // (c_g >= 0 keeps the order)
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
@@ -322,81 +353,115 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tile_max = fmaxf(tile_max, a * cg[g]);
           }
         } else {
-          // masked tile: scale each score; -inf where the key is past the end or causal-masked
+          // causal diagonal or ragged tail: 32 columns at a time from tensor memory, keys past
+          // the row's limit excluded
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t t[32];
+            tmem_ld32(tS + ch * 32, t);
+            tmem_wait_ld(t);
+            const float c0 = pick8(cg, 2 * ch), c1 = pick8(cg, 2 * ch + 1);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int kj = kv0 + c;
-            const bool allowed = kj < s.len_k && (!p.is_causal || kj <= i);
-            const float t = allowed ? __uint_as_float(sr[c >> 5][c & 31]) * cg[c >> 4]
-                                    : __int_as_float(0xff800000);
-            sr[c >> 5][c & 31] = __float_as_uint(t);
-            tile_max = fmaxf(tile_max, t);
+            for (int u = 0; u < 32; ++u)
+              if (ch * 32 + u < limit)
+                tile_max = fmaxf(tile_max, __uint_as_float(t[u]) * (u < 16 ? c0 : c1));
           }
+          trace(p, trs, x, j, 1);
         }
+        trace(p, trs, x, j, 2);
         const float m_new = fmaxf(m, tile_max);
         const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
         const float bias = log2_sigma - m_use;
-        // P~ = e4m3(2^(x - m) * sigma), packed 4 per word, and the row sum; two scores per
-        // packed fp32 instruction
-        uint32_t pk[32];
-        float gsum[16];  // a pair of partial row sums per 16-key sub-group
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int c = g * 16; c < g * 16 + 16; c += 4) {
-            float x0, x1, x2, x3;
-            const float s0 = __uint_as_float(sr[c >> 5][c & 31]);
-            const float s1 = __uint_as_float(sr[c >> 5][(c & 31) + 1]);
-            const float s2 = __uint_as_float(sr[c >> 5][(c & 31) + 2]);
-            const float s3 = __uint_as_float(sr[c >> 5][(c & 31) + 3]);
-            if (!need_mask) {
-              fma2(x0, x1, s0, s1, cg[g], cg[g], bias, bias);
-              fma2(x2, x3, s2, s3, cg[g], cg[g], bias, bias);
-            } else {
-              add2(x0, x1, s0, s1, bias, bias);
-              add2(x2, x3, s2, s3, bias, bias);
-            }
-            const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
-            add2(a0, a1, a0, a1, e0, e1);
-            add2(a0, a1, a0, a1, e2, e3);
-            pk[c / 4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
-          }
-          gsum[2 * g] = a0;
-          gsum[2 * g + 1] = a1;
-        }
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int u = 0; u < w; ++u) gsum[u] += gsum[u + w];
-        const float rs = gsum[0];
-        l = l * alpha + rs;
-        m = m_new;
-        // P tile buffer and O are free once the previous P.V of this tile has completed
+        // the P buffer is free once the previous P.V of this tile has completed
         if (j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
         }
+        trace(p, trs, x, j, 4);
+        // P~ = e4m3(2^(x - m) * sigma) written 16 keys (one 16-byte chunk, 128-byte swizzle)
+        // at a time; the row sum uses four independent accumulator pairs
+        float gsum[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 val = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-          *reinterpret_cast<uint4*>(my_p + ((ch ^ (r & 7)) << 4)) = val;
+        for (int u = 0; u < 8; ++u) gsum[u] = 0.f;
+        if (!masked) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float a0 = 0.f, a1 = 0.f;
+            uint32_t w4[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int c = g * 16 + q4 * 4;
+              float x0, x1, x2, x3;
+              fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
+                   cg[g], cg[g], bias, bias);
+              fma2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
+                   cg[g], cg[g], bias, bias);
+              const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+              add2(a0, a1, a0, a1, e0, e1);
+              add2(a0, a1, a0, a1, e2, e3);
+              w4[q4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
+            }
+            *reinterpret_cast<uint4*>(my_p + ((g ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
+          }
+        } else {
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t t[32];
+            tmem_ld32(tS + ch * 32, t);
+            tmem_wait_ld(t);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const float cgc = pick8(cg, 2 * ch + half);
+              uint32_t w4[4];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                float e[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const int u = half * 16 + q4 * 4 + v;
+                  e[v] = ch * 32 + u < limit ? ex2(fmaf(__uint_as_float(t[u]), cgc, bias)) : 0.f;
+                }
+                add2(a0, a1, a0, a1, e[0], e[1]);
+                add2(a0, a1, a0, a1, e[2], e[3]);
+                w4[q4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
+              }
+              *reinterpret_cast<uint4*>(my_p + (((2 * ch + half) ^ (r & 7)) << 4)) =
+                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            gsum[0] += a0;
+            gsum[1] += a1;
+          }
         }
+        const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
+        // next tile's K scales (used one tile from now)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int kg = kv0 + kTileKeys + g * 16;
+          skn[g] = kg < s.len_k ? __ldg(&skp[kg >> lgk]) : 0.f;
+        }
+        trace(p, trs, x, j, 3);
+        l = l * alpha + rs;
+        m = m_new;
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
+        trace(p, trs, x, j, 5);
         // rescale this warp's O rows for the grown max while the next scores are computed;
         // P_j(x) V_j is issued only after o_ready
         if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
-          uint32_t o[DP / 32][32];
 #pragma unroll
-          for (int cc = 0; cc < DP / 32; ++cc) tmem_ld32(tO + cc * 32, o[cc]);
+          for (int c2 = 0; c2 < DP / 64; ++c2) {
+          uint32_t o[2][32];
 #pragma unroll
-          for (int cc = 0; cc < DP / 32; ++cc) tmem_wait_ld(o[cc]);
+          for (int cc = 0; cc < 2; ++cc) tmem_ld32(tO + (c2 * 2 + cc) * 32, o[cc]);
 #pragma unroll
-          for (int cc = 0; cc < DP / 32; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) tmem_wait_ld(o[cc]);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
             for (int u = 0; u < 32; u += 2) {
               float a0, a1;
@@ -404,12 +469,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               o[cc][u] = __float_as_uint(a0);
               o[cc][u + 1] = __float_as_uint(a1);
             }
-            tmem_st32(tO + cc * 32, o[cc]);
+            tmem_st32(tO + (c2 * 2 + cc) * 32, o[cc]);
+          }
           }
           tmem_wait_st();
         }
         tc_fence_before();
         mbar_arrive(&o_ready[x]);
+        trace(p, trs, x, j, 6);
       }
       // ---- epilogue
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (n_tiles - 1) & 1, abort_flag));

@@ -21,7 +21,7 @@ struct Problem {
   int batch, hq, hkv, d, dp;       // dp: padded head_dim (64 or 128)
   int nq, nk;                      // dense: sequence lengths; varlen: max lengths
   int varlen, dtype, is_causal, return_lse, smooth_k, smooth_v;
-  int gq, gk;                      // token-group sizes of Q and K scales
+  int gq, gk, lgk;                 // token-group sizes of Q and K scales; lgk = log2(gk)
   int acc_mode;                    // 0: fp32 (P scaled by 448), 1: fp16 partials + fp32
   int vec16;                       // inputs allow 16-byte vector loads
   float sm_scale;
@@ -46,7 +46,10 @@ struct Problem {
   int64_t sq_pp, sk_pp;            // scale groups per plane
   int32_t* dbg_scores;             // optional exact-score dump [B,Hq,Nq,Nk]
   int dbg_stall;                   // test hook: the producer issues no K/V loads
+  long long* dbg_trace;            // optional event clocks of CTA (0,0,0): [4 roles][64 tiles][8]
 };
+
+constexpr int kTraceTiles = 64, kTraceEvents = 8;
 
 struct Seq {
   int tok0_q, len_q, row0_q, tok0_k, len_k, row0_k;

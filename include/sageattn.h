@@ -106,6 +106,32 @@ int sage_attn(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
               int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
               size_t workspace_bytes, void* stream);
 
+/* Capacity of the scratch array built into the library for sage_attn_no_alloc. */
+#define SAGE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* sage_attn without a caller-supplied workspace and without any device allocation.
+ * (The pages have no counterpart; this exists for callers that cannot allocate.)
+ * Some callers cannot call cudaMalloc where they run attention: a plugin executing inside a
+ * host engine that gives it only its input/output buffers and forbids allocation while it
+ * runs, or a latency-critical path that cannot afford an allocation's time or failure. This
+ * entry point takes its scratch from a fixed array of SAGE_NO_ALLOC_SCRATCH_BYTES bytes
+ * compiled into the library (held by every GPU that loads the library until the process
+ * exits); the caller still passes inputs, outputs and the optional LSE buffer.
+ *   Arguments, layouts and results are those of sage_attn.
+ *   Returns SAGE_ERR_WORKSPACE, before launching anything, when the problem needs more than
+ *   SAGE_NO_ALLOC_SCRATCH_BYTES of scratch (sage_attn_workspace_size tells how much).
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current); make that first call before any stream capture.
+ *   Every call on a device uses the same array: calls that may overlap on the GPU (other
+ *   streams, other host threads) race and must be serialised by the caller. Each call
+ *   clears what it needs cleared; nothing an earlier call left in the array is read.
+ *   Calls no cudaMalloc, cudaFree or allocating library routine. */
+int sage_attn_no_alloc(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                       const sage_tensor* out, float* lse, int batch, int heads_q, int heads_kv,
+                       int seqlen_q, int seqlen_k, int head_dim, int dtype, int tensor_layout,
+                       int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+                       int pv_accum_dtype, int smooth_k, int smooth_v, void* stream);
+
 /* Bytes of workspace sage_attn_varlen needs (0 on invalid sizes). */
 size_t sage_attn_varlen_workspace_size(int batch, int heads_q, int heads_kv, int total_q,
                                        int total_k, int head_dim, int qk_quant_gran);

@@ -212,7 +212,7 @@ def run_reference(args, w):
 def run_ours(args, w):
     import torch
     import quantized_attention_mean_gb300 as qa
-    from quantized_attention_mean_gb300.workloads import dense_inputs
+    from quantized_attention_mean_gb300.workloads import dense_inputs, varlen_inputs
 
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -221,31 +221,44 @@ def run_ours(args, w):
     pk = peaks()
 
     # resident input sets: enough that one pass over them exceeds L2
-    q0, k0, v0 = dense_inputs(w, seed=rank)
+    if w.varlen:
+        q0, k0, v0, cu0, _, lens = varlen_inputs(w, seed=0)
+        wsb = qa.varlen_workspace_bytes(len(lens), w.Hq, w.Hkv, q0.shape[0], k0.shape[0], w.d, w.gran)
+    else:
+        q0, k0, v0 = dense_inputs(w, seed=rank)
+        wsb = qa.workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran)
     per_set = sum(t.numel() * t.element_size() for t in (q0, k0, v0)) * 4 // 3  # + output
-    wsb = qa.workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran)
     nsets = max(2, -(-2 * L2_BYTES // (per_set + wsb)))
     sets = []
     for i in range(nsets):
-        q, k, v = (t.to(dev) for t in dense_inputs(w, seed=rank * 100 + i))
+        if w.varlen:
+            q, k, v, cu, _, _ = varlen_inputs(w, seed=0, lengths=lens)
+            q, k, v, cu = (t.to(dev) for t in (q, k, v, cu))
+            lse = torch.empty((w.Hq, q.shape[0]), dtype=torch.float32, device=dev) if w.return_lse else None
+        else:
+            q, k, v = (t.to(dev) for t in dense_inputs(w, seed=rank * 100 + i))
+            cu = None
+            lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev) if w.return_lse else None
         out = torch.empty_like(q)
-        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev) if w.return_lse else None
         ws = qa.alloc_workspace(wsb, dev)
-        sets.append((q, k, v, out, lse, ws))
-    kw = dict(tensor_layout=w.layout, is_causal=w.is_causal, return_lse=w.return_lse,
-              qk_quant_gran=w.gran, pv_accum_dtype=w.accum, smooth_k=w.smooth_k, smooth_v=w.smooth_v)
+        sets.append((q, k, v, out, lse, ws, cu))
+    kw = dict(is_causal=w.is_causal, return_lse=w.return_lse, qk_quant_gran=w.gran,
+              pv_accum_dtype=w.accum, smooth_k=w.smooth_k, smooth_v=w.smooth_v)
     stream = torch.cuda.current_stream()
 
     def step(i):
-        q, k, v, out, lse, ws = sets[i % nsets]
-        qa.sage_attn(q, k, v, out=out, lse=lse, workspace=ws, **kw)
+        q, k, v, out, lse, ws, cu = sets[i % nsets]
+        if w.varlen:
+            qa.sage_attn_varlen(q, k, v, cu, cu, max(lens), max(lens), out=out, lse=lse, workspace=ws, **kw)
+        else:
+            qa.sage_attn(q, k, v, tensor_layout=w.layout, out=out, lse=lse, workspace=ws, **kw)
 
     for i in range(max(3, args.warmup)):
         step(i)
     torch.cuda.synchronize()
     assert qa.read_device_status(sets[0][5]) == 0
 
-    ops = w.ops()
+    ops = w.ops(lens) if w.varlen else w.ops()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
@@ -283,7 +296,7 @@ def run_ours(args, w):
 
     # end to end through the public API with pinned host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not w.varlen:
         hq, hk, hv = (t.pin_memory() for t in dense_inputs(w, seed=rank))
         ho = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
         dq, dk, dv = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev)
@@ -316,7 +329,7 @@ def run_ours(args, w):
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     cpu = None
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline and not w.varlen:
         rows = w.Nq  # one full head
         c_ops, c_s = cpu_baseline_subprocess(w.name, rows)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -335,7 +348,8 @@ def run_ours(args, w):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 7 * args.steps,  # reset, stats, finalize, quant Q/K/V, attention
+            # reset, stats, finalize, quant Q/K/V, attention (+ varlen set-up)
+            "gpu_launches": (8 if w.varlen else 7) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -348,8 +362,6 @@ def main():
     args = parse()
     from quantized_attention_mean_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
-    if w.varlen:
-        raise SystemExit("bench: varlen workloads are measured by tests, not this entry point")
     if args.impl == "reference":
         run_reference(args, w)
     else:

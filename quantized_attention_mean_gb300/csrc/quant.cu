@@ -80,15 +80,16 @@ __global__ void ws_reset_kernel(Problem p, int n_stats) {
 // ------------------------------------------------------------------------------------------
 // K/V statistics: fixed-point sums of K and V (smooth_k / smooth_v) and the min / max of V
 // per (sequence, kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads:
-// thread = (row group rg in 0..15, channel vector vec in 0..15).
-template <typename T>
+// thread = (row group rg, channel vector vec); TPR = padded head_dim / 8 threads per row.
+template <typename T, int TPR>
 __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
+  constexpr int RG = 256 / TPR;
   const int chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int t0 = chunk * kStatsChunk;
   if (t0 >= s.len_k) return;
   const int t1 = min(t0 + kStatsChunk, s.len_k);
-  const int vec = threadIdx.x & 15, rg = threadIdx.x >> 4;
+  const int vec = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = vec * 8;
   const bool active = c0 < p.d;
   const float lim = p.varlen ? __double2float_ru(__ddiv_rn(274877906944.0, (double)s.len_k))
@@ -106,11 +107,11 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
   const T* vp = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
   if (active) {
     // every row of this thread (8 rows x K and V) is requested before any is used
-    constexpr int kRows = kStatsChunk / 16;
+    constexpr int kRows = kStatsChunk / RG;
     uint4 kr[kRows], vr[kRows];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-      const int t = t0 + rg + 16 * r;
+      const int t = t0 + rg + RG * r;
       const int64_t tok = (int64_t)(s.tok0_k + t);
       const bool valid = t < t1;
       vr[r] = valid ? load8_raw<T>(vp + tok * p.v_sn, c0, p.d, p.vec16) : make_uint4(0, 0, 0, 0);
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
     }
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-      if (t0 + rg + 16 * r >= t1) continue;
+      if (t0 + rg + RG * r >= t1) continue;
       float vx[8], kx[8];
       unpack8<T>(vr[r], vx);
       unpack8<T>(kr[r], kx);
@@ -139,20 +140,23 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
     }
   }
   if (range_bad) record_error(p.err, kDevRange);
-  // reduce the two row groups that share a warp, then the 8 warps through shared memory
+  // reduce the row groups that share a warp, then the 8 warps through shared memory
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], 16);
-    vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], 16);
-    vmn[i] = fminf(vmn[i], __shfl_xor_sync(0xffffffffu, vmn[i], 16));
-    vmx[i] = fmaxf(vmx[i], __shfl_xor_sync(0xffffffffu, vmx[i], 16));
+  for (int off = TPR; off < 32; off <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], off);
+      vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], off);
+      vmn[i] = fminf(vmn[i], __shfl_xor_sync(0xffffffffu, vmn[i], off));
+      vmx[i] = fmaxf(vmx[i], __shfl_xor_sync(0xffffffffu, vmx[i], off));
+    }
   }
   __shared__ long long red_s[8][128];
   __shared__ float red_f[8][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t sidx = ((int64_t)b * p.hkv + hk) * p.d;
   // pass 1: K sums
-  if (lane < 16) {
+  if (lane < TPR) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = ks[i];
   }
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
   }
   __syncthreads();
   // pass 2: V sums
-  if (lane < 16) {
+  if (lane < TPR) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = vs[i];
   }
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
               static_cast<unsigned long long>(acc));
   }
   // pass 3: V min
-  if (lane < 16) {
+  if (lane < TPR) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmn[i];
   }
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
   }
   __syncthreads();
   // pass 4: V max
-  if (lane < 16) {
+  if (lane < TPR) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmx[i];
   }
@@ -234,8 +238,10 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //   V: V' = V - vmean, E4M3 with the per-channel scale absmax/448, written transposed
 //      [channel][token] so that P.V reads V^T tiles K-major.
 // Rows past the sequence end up to the stored tile end are written as zeros.
-template <typename T, int kind>
+template <typename T, int kind, int TPR>
 __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
+  constexpr int RG = 256 / TPR;      // row groups
+  constexpr int RPT = kTileRows / RG;  // rows per thread
   const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int len = kind == 0 ? s.len_q : s.len_k;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
   const int stored = p.varlen ? (len + kTileRows - 1) / kTileRows * kTileRows : len;
   const int r0 = tile * kTileRows;
   if (r0 >= stored) return;
-  const int vec = threadIdx.x & 15, rg = threadIdx.x >> 4;
+  const int vec = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = vec * 8;
   const int d = p.d, dp = p.dp;
   const int hk = kind == 0 ? h / (p.hq / p.hkv) : h;   // kv head feeding this q head
@@ -278,17 +284,17 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
     base = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)h * p.v_sh; sn = p.v_sn;
   }
   const int tok0 = kind == 0 ? s.tok0_q : s.tok0_k;
-  uint4 raw[8];
+  uint4 raw[RPT];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = r0 + rg + 16 * i;
+  for (int i = 0; i < RPT; ++i) {
+    const int r = r0 + rg + RG * i;
     raw[i] = (r < len && c0 < d) ? load8_raw<T>(base + (int64_t)(tok0 + r) * sn, c0, d, p.vec16)
                                  : make_uint4(0, 0, 0, 0);
   }
   // smoothed fp32 values of row i (x - mean, one IEEE subtraction; 0 past the end / past d)
   auto row_values = [&](int i, float (&x)[8]) {
     unpack8<T>(raw[i], x);
-    const bool live = r0 + rg + 16 * i < len;
+    const bool live = r0 + rg + RG * i < len;
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = (live && c0 + j < d) ? __fsub_rn(x[j], mean[j]) : 0.f;
   };
@@ -296,8 +302,8 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
   if (kind == 2) {
     // ---- V: E4M3 codes, transposed through shared memory
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = rg + 16 * i;
+    for (int i = 0; i < RPT; ++i) {
+      const int rr = rg + RG * i;
       float x[8];
       row_values(i, x);
 #pragma unroll
@@ -329,17 +335,15 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
   // ---- Q / K: INT8 codes per token group
   const int gs = kind == 0 ? p.gq : p.gk;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < RPT; ++i) {
     float x[8];
     row_values(i, x);
     float a = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    if (vec == 0) rowmax[rg + 16 * i] = a;
+#pragma unroll
+    for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    if (vec == 0) rowmax[rg + RG * i] = a;
   }
   __syncthreads();
   const int64_t plane = plane_of(p, b, h, kind == 0 ? p.hq : p.hkv);
@@ -378,8 +382,8 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
   __half* codes = kind == 0 ? p.qc : p.kc;
   const int64_t rows_pp = kind == 0 ? p.q_rows : p.k_rows;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = rg + 16 * i;
+  for (int i = 0; i < RPT; ++i) {
+    const int rr = rg + RG * i;
     const int r = r0 + rr;
     const float rc = grcp[rr / gs];
     float x[8];
@@ -398,10 +402,8 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
       float dot = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) dot = fmaf(x[j], kmean_q[j], dot);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+#pragma unroll
+      for (int off = 1; off < TPR; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       if (vec == 0 && r < len) p.qkc[plane * p.q_rows + row0 + r] = dot;
     }
   }
@@ -448,10 +450,16 @@ cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <typename T>
+static void launch_kv_stats_t(const Problem& p, dim3 grid, cudaStream_t st) {
+  if (p.dp == 64) kv_stats_kernel<T, 8><<<grid, 256, 0, st>>>(p);
+  else kv_stats_kernel<T, 16><<<grid, 256, 0, st>>>(p);
+}
+
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
   const dim3 grid((max_len_k + kStatsChunk - 1) / kStatsChunk, p.hkv, p.batch);
-  if (p.dtype == 0) kv_stats_kernel<__half><<<grid, 256, 0, st>>>(p);
-  else kv_stats_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  if (p.dtype == 0) launch_kv_stats_t<__half>(p, grid, st);
+  else launch_kv_stats_t<__nv_bfloat16>(p, grid, st);
   return cudaGetLastError();
 }
 
@@ -464,9 +472,15 @@ template <typename T>
 static void launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
   const dim3 gq((max_len_q + kTileRows - 1) / kTileRows, p.hq, p.batch);
   const dim3 gk((max_len_k + kTileRows - 1) / kTileRows, p.hkv, p.batch);
-  quant_kernel<T, 0><<<gq, 256, 0, st>>>(p);
-  quant_kernel<T, 1><<<gk, 256, 0, st>>>(p);
-  quant_kernel<T, 2><<<gk, 256, 0, st>>>(p);
+  if (p.dp == 64) {
+    quant_kernel<T, 0, 8><<<gq, 256, 0, st>>>(p);
+    quant_kernel<T, 1, 8><<<gk, 256, 0, st>>>(p);
+    quant_kernel<T, 2, 8><<<gk, 256, 0, st>>>(p);
+  } else {
+    quant_kernel<T, 0, 16><<<gq, 256, 0, st>>>(p);
+    quant_kernel<T, 1, 16><<<gk, 256, 0, st>>>(p);
+    quant_kernel<T, 2, 16><<<gk, 256, 0, st>>>(p);
+  }
 }
 
 cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {

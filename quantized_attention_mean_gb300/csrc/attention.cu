@@ -6,7 +6,8 @@
 // KV tiles of 128 keys:
 //   warp 8      TMA producer: Q tiles once, then K tiles (integer-valued fp16 codes) and
 //               V^T tiles (E4M3) through a ring of shared-memory stages;
-//   warp 9      allocates tensor memory and issues the MMAs from one thread:
+//   warp 9      allocates tensor memory and issues the MMAs from one thread (A and B
+//               alternating):
 //               S = Q8 . K8^T  (tcgen05 kind::f16 on the INT8 codes: every product and partial
 //                               sum is an integer below 2^24, so the fp32 accumulator holds
 //                               the exact INT32 score),
@@ -48,7 +49,7 @@ struct AttnCfg {
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 1;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
@@ -59,6 +60,7 @@ struct AttnCfg {
 __host__ __device__ constexpr uint32_t idesc_qk() { return make_idesc(1, 0, 0, 128, 128); }
 template <int DP>
 __host__ __device__ constexpr uint32_t idesc_pv() { return make_idesc(1, 0, 0, 128, DP); }
+
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -72,6 +74,76 @@ __device__ __forceinline__ float pick8(const float (&a)[8], int idx) {
 #pragma unroll
   for (int g = 1; g < 8; ++g) v = idx == g ? a[g] : v;
   return v;
+}
+
+// ---- rarely taken softmax paths, kept out of line so the hot loop stays small in the
+// instruction cache. They re-read S from tensor memory 32 columns at a time.
+struct Mult8 {
+  float v[8];
+};
+
+// Test hook: the integer scores of one row of the tile as read from tensor memory.
+__device__ __noinline__ void dump_scores_row(uint32_t tS, bool row_valid, int32_t* dst, int ncols) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t t[32];
+    tmem_ld32(tS + ch * 32, t);
+    tmem_wait_ld(t);
+    if (row_valid) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (ch * 32 + u < ncols) dst[ch * 32 + u] = __float2int_rn(__uint_as_float(t[u]));
+    }
+  }
+}
+
+// Max over the keys [0, limit) of the tile of S * c (c per 16-key sub-group).
+__device__ __noinline__ float masked_tile_max(uint32_t tS, int limit, Mult8 cg) {
+  float tile_max = __int_as_float(0xff800000);
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t t[32];
+    tmem_ld32(tS + ch * 32, t);
+    tmem_wait_ld(t);
+    const float c0 = pick8(cg.v, 2 * ch), c1 = pick8(cg.v, 2 * ch + 1);
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      if (ch * 32 + u < limit) tile_max = fmaxf(tile_max, __uint_as_float(t[u]) * (u < 16 ? c0 : c1));
+  }
+  return tile_max;
+}
+
+// P~ = e4m3(2^(S*c + bias)) for keys [0, limit) (0 beyond), written to the row's swizzled
+// P buffer; returns the row sum of the unquantised values.
+__device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, float bias,
+                                              uint8_t* my_p, int r) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t t[32];
+    tmem_ld32(tS + ch * 32, t);
+    tmem_wait_ld(t);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const float cgc = pick8(cg.v, 2 * ch + half);
+      uint32_t w4[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float e[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int u = half * 16 + q4 * 4 + v;
+          e[v] = ch * 32 + u < limit ? ex2(fmaf(__uint_as_float(t[u]), cgc, bias)) : 0.f;
+        }
+        add2(a0, a1, a0, a1, e[0], e[1]);
+        add2(a0, a1, a0, a1, e[2], e[3]);
+        w4[q4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
+      }
+      *reinterpret_cast<uint4*>(my_p + (((2 * ch + half) ^ (r & 7)) << 4)) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+  }
+  return a0 + a1;
 }
 
 // Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0).
@@ -102,7 +174,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* p_full = s_full + 2;             // [2]
   uint64_t* o_full = p_full + 2;             // [2]
   uint64_t* o_ready = o_full + 2;            // [2]
-  uint64_t* drain = o_ready + 2;
+  uint64_t* drain = o_ready + 2;             // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
 
@@ -138,7 +210,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&o_full[i], 1);
       mbar_init(&o_ready[i], 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -206,25 +279,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
    } else if (warp == 9) {
     // =========================================================== MMA issuer
+    // one thread issues both query tiles' MMAs, alternating A and B, so the two tiles' softmax
+    // phases stay offset by half an iteration and the tensor core serves one while the other
+    // computes
     if (lane == 0) {
-      const uint32_t sq_addr = smem_u32(sQ), sk_addr = smem_u32(sK), sv_addr = smem_u32(sV),
-                     sp_addr = smem_u32(sP);
       const int nx = has_b ? 2 : 1;
+      // descriptor bases; a K step inside a 128-byte row adds its byte offset / 16 to the
+      // start-address field (no carry: shared-memory addresses stay below 2^18)
+      const uint64_t dq = sdesc_sw128(smem_u32(sQ));
+      const uint64_t dk = sdesc_sw128(smem_u32(sK));
+      const uint64_t dp = sdesc_sw128(smem_u32(sP));
+      const uint64_t dv = sdesc_sw128(smem_u32(sV));
       auto issue_qk = [&](int x, int st) {
-        const uint32_t qa = sq_addr + x * C::kQTileBytes, ka = sk_addr + st * C::kKTileBytes;
+        const uint32_t d_s = tmem + (x ? 128u : 0u);
+        const uint64_t qx = dq + static_cast<uint64_t>((x * C::kQTileBytes) >> 4);
+        const uint64_t kst = dk + static_cast<uint64_t>((st * C::kKTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < DP / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kTileRows * 128) + (k & 3) * 32;
-          mma_f16_ss(tmem + (x ? 128u : 0u), sdesc_sw128(qa + off), sdesc_sw128(ka + off), idesc_qk(), k > 0);
+          const uint32_t off = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
+          mma_f16_ss(d_s, qx + off, kst + off, idesc_qk(), k > 0);
         }
         mma_commit(&s_full[x]);
       };
       auto issue_pv = [&](int x, int sv, bool first) {
-        const uint32_t pa = sp_addr + x * C::kPTileBytes, va = sv_addr + sv * C::kVTileBytes;
+        const uint32_t d_o = tmem + (x ? 384u : 256u);
+        const uint64_t px = dp + static_cast<uint64_t>((x * C::kPTileBytes) >> 4);
+        const uint64_t vst = dv + static_cast<uint64_t>((sv * C::kVTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kTileKeys / 32; ++k)
-          mma_f8_ss(tmem + (x ? 384u : 256u), sdesc_sw128(pa + k * 32), sdesc_sw128(va + k * 32), idesc_pv<DP>(),
-                    (!first || k > 0) ? 1u : 0u);
+          mma_f8_ss(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
         mma_commit(&o_full[x]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(&k_full[0], 0, abort_flag);
@@ -264,9 +347,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mma_commit(&v_empty[sv]);
       }
       // every MMA must have finished before tensor memory is released
-      mma_commit(drain);
+      mma_commit(&drain[0]);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never);
+      mbar_wait(&drain[0], 0, &never);
       if (!ok) record_error(p.err, kDevTimeout);
     }
    }
@@ -308,21 +391,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kv0 = j * kTileKeys;
         const int limit = row_limit - kv0;  // this row's allowed keys in the tile: [0, limit)
         const bool masked = __any_sync(0xffffffffu, limit < kTileKeys);
-        if (p.dbg_scores != nullptr) {
-          // test hook: the integer scores as read from tensor memory
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t t[32];
-            tmem_ld32(tS + ch * 32, t);
-            tmem_wait_ld(t);
-            if (row_valid) {
-              int32_t* dst = p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk + kv0 + ch * 32;
-#pragma unroll
-              for (int u = 0; u < 32; ++u)
-                if (kv0 + ch * 32 + u < s.len_k) dst[u] = __float2int_rn(__uint_as_float(t[u]));
-            }
-          }
-        }
+        if (__builtin_expect(p.dbg_scores != nullptr, 0))
+          dump_scores_row(tS, row_valid, p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk + kv0,
+                          min(kTileKeys, s.len_k - kv0));
         // multipliers c_g = s_q * s_k * sm_scale * log2(e) for the 8 sub-groups of 16 keys
         // (a K scale group is 16 or 64 keys, so each sub-group has one scale)
         float cg[8];
@@ -330,7 +401,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int g = 0; g < 8; ++g) cg[g] = row_scale * skn[g];
         uint32_t sr[4][32];
         float tile_max = __int_as_float(0xff800000);
-        if (!masked) {
+        if (__builtin_expect(!masked, 1)) {
           // every key of the tile is visible: scores stay in registers
           tmem_ld32(tS + 0, sr[0]);
           tmem_ld32(tS + 32, sr[1]);
@@ -353,19 +424,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tile_max = fmaxf(tile_max, a * cg[g]);
           }
         } else {
-          // causal diagonal or ragged tail: 32 columns at a time from tensor memory, keys past
-          // the row's limit excluded
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t t[32];
-            tmem_ld32(tS + ch * 32, t);
-            tmem_wait_ld(t);
-            const float c0 = pick8(cg, 2 * ch), c1 = pick8(cg, 2 * ch + 1);
+          // causal diagonal or ragged tail: keys past the row's limit excluded
+          Mult8 c8;
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-              if (ch * 32 + u < limit)
-                tile_max = fmaxf(tile_max, __uint_as_float(t[u]) * (u < 16 ? c0 : c1));
-          }
+          for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
+          tile_max = masked_tile_max(tS, limit, c8);
           trace(p, trs, x, j, 1);
         }
         trace(p, trs, x, j, 2);
@@ -385,7 +448,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float gsum[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) gsum[u] = 0.f;
-        if (!masked) {
+        if (__builtin_expect(!masked, 1)) {
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             float a0 = 0.f, a1 = 0.f;
@@ -407,34 +470,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
           }
         } else {
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t t[32];
-            tmem_ld32(tS + ch * 32, t);
-            tmem_wait_ld(t);
-            float a0 = 0.f, a1 = 0.f;
+          Mult8 c8;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const float cgc = pick8(cg, 2 * ch + half);
-              uint32_t w4[4];
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                float e[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const int u = half * 16 + q4 * 4 + v;
-                  e[v] = ch * 32 + u < limit ? ex2(fmaf(__uint_as_float(t[u]), cgc, bias)) : 0.f;
-                }
-                add2(a0, a1, a0, a1, e[0], e[1]);
-                add2(a0, a1, a0, a1, e[2], e[3]);
-                w4[q4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
-              }
-              *reinterpret_cast<uint4*>(my_p + (((2 * ch + half) ^ (r & 7)) << 4)) =
-                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-            gsum[0] += a0;
-            gsum[1] += a1;
-          }
+          for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
+          gsum[0] = masked_tile_exp(tS, limit, c8, bias, my_p, r);
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
         // next tile's K scales (used one tile from now)

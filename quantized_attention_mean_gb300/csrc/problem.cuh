@@ -2,6 +2,7 @@
 // small device helpers (input loads, per-sequence geometry, FP8 packing, error recording).
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -9,7 +10,8 @@ namespace sage {
 
 constexpr int kTileRows = 128;   // query rows per attention tile, tokens per quantisation tile
 constexpr int kTileKeys = 128;   // keys per attention KV tile
-constexpr int kStatsChunk = 128; // tokens per block in the K/V statistics pass
+// tokens per block in the K/V statistics pass (4 rows per thread, dp/8 threads per row)
+__host__ __device__ constexpr int stats_chunk(int dp) { return 8192 / dp; }
 
 // Device-side status codes (mirror sage_status in include/sageattn.h).
 enum DevStatus : int { kDevOk = 0, kDevRange = 7, kDevTimeout = 9, kDevSeqlens = 12 };
@@ -129,6 +131,42 @@ __device__ __forceinline__ int float_to_ordered(float f) {
 }
 __device__ __forceinline__ float ordered_to_float(int i) {
   return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF);
+}
+
+// Adding 1.5 * 2^23 rounds an fp32 value v with |v| < 2^22 to an integer (ties to even, the
+// IEEE default), which the sum then holds in its low mantissa bits: the integer is
+// bits(v + 1.5 * 2^23) - bits(1.5 * 2^23). This replaces float -> int conversions, which run on
+// a slow pipe (fp32 -> int64 at ~2 per clock per SM on this GPU).
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kRoundMagicBits = 0x4B400000;
+
+// x * 2^24 split exactly into hi * 2^20 + lo with hi = round(x * 16), lo = (x * 16 - hi) * 2^20.
+// Exact whenever x * 2^24 is an integer and |x| < 2^18 (every fp16 value; bf16 values of
+// magnitude >= 2^-17 or 0): then r = x * 16 - hi is exact and r * 2^20 is an integer < 2^19.
+__device__ __forceinline__ void fixed_split(float x, int& hi, int& lo) {
+  const float t1 = __fmaf_rn(x, 16.0f, kRoundMagic);
+  hi = __float_as_int(t1) - kRoundMagicBits;
+  const float r = __fmaf_rn(x, 16.0f, -__fsub_rn(t1, kRoundMagic));
+  lo = __float_as_int(__fmaf_rn(r, 1048576.0f, kRoundMagic)) - kRoundMagicBits;
+}
+template <typename T>
+__device__ __forceinline__ bool fixed_split_exact(float x) {
+  if (std::is_same<T, __half>::value) return true;  // |x| <= 65504, multiples of 2^-24
+  const float a = fabsf(x);
+  return a < 262144.0f && (a >= 7.62939453125e-06f || a == 0.0f);
+}
+// Adds trunc(x * 2^24) to the (hi, lo, slow) accumulators; values the split cannot take
+// exactly go through the int64 conversion.
+template <typename T>
+__device__ __forceinline__ void fixed_accumulate(float x, int& hi, int& lo, long long& slow) {
+  if (fixed_split_exact<T>(x)) {
+    int h, l;
+    fixed_split(x, h, l);
+    hi += h;
+    lo += l;
+  } else {
+    slow += __float2ll_rz(x * 16777216.0f);
+  }
 }
 
 // Exact, order-free mean from the fixed-point sum: fl32(fl64(fl64(S) * 2^-24 / n)).

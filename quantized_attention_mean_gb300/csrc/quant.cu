@@ -78,130 +78,142 @@ __global__ void ws_reset_kernel(Problem p, int n_stats) {
 }
 
 // ------------------------------------------------------------------------------------------
-// K/V statistics: fixed-point sums of K and V (smooth_k / smooth_v) and the min / max of V
-// per (sequence, kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads:
-// thread = (row group rg, channel vector vec); TPR = padded head_dim / 8 threads per row.
-template <typename T, int TPR>
-__global__ void __launch_bounds__(256, 2) kv_stats_kernel(Problem p) {
+// K/V statistics, one tensor per launch (KIND 0: K, the fixed-point sum, launched only with
+// smooth_k; KIND 1: V, the fixed-point sum with smooth_v, and the min / max). Per (sequence,
+// kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads: thread = (row group rg,
+// channel vector vec); TPR = padded head_dim / 8 threads per row.
+template <typename T, int TPR, int KIND>
+__global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
   constexpr int RG = 256 / TPR;
+  constexpr int kRows = 4;                 // rows per thread
+  constexpr int kChunk = kRows * RG;       // tokens per block: stats_chunk(8 * TPR)
   const int chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
-  const int t0 = chunk * kStatsChunk;
+  const int t0 = chunk * kChunk;
   if (t0 >= s.len_k) return;
-  const int t1 = min(t0 + kStatsChunk, s.len_k);
+  const int t1 = min(t0 + kChunk, s.len_k);
   const int vec = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = vec * 8;
   const bool active = c0 < p.d;
+  const bool want_sum = KIND == 0 || p.smooth_v;
   const float lim = p.varlen ? __double2float_ru(__ddiv_rn(274877906944.0, (double)s.len_k))
                              : p.range_limit;
-  long long ks[8], vs[8];
-  float vmn[8], vmx[8];
+  const T* base = KIND == 0
+      ? static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh
+      : static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
+  const int64_t sn = KIND == 0 ? p.k_sn : p.v_sn;
+  int hi[8], lo[8];
+  float mn[8], mx[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    ks[i] = 0; vs[i] = 0;
-    vmn[i] = __int_as_float(0x7f800000);
-    vmx[i] = __int_as_float(0xff800000);
+    hi[i] = lo[i] = 0;
+    mn[i] = __int_as_float(0x7f800000);
+    mx[i] = __int_as_float(0xff800000);
   }
+  bool exact = true;  // every value went through the exact int32 split
   bool range_bad = false;
-  const T* kp = static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh;
-  const T* vp = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
   if (active) {
-    // every row of this thread (8 rows x K and V) is requested before any is used
-    constexpr int kRows = kStatsChunk / RG;
-    uint4 kr[kRows], vr[kRows];
+    // every row of this thread is requested before any is used
+    uint4 raw[kRows];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
       const int t = t0 + rg + RG * r;
-      const int64_t tok = (int64_t)(s.tok0_k + t);
-      const bool valid = t < t1;
-      vr[r] = valid ? load8_raw<T>(vp + tok * p.v_sn, c0, p.d, p.vec16) : make_uint4(0, 0, 0, 0);
-      kr[r] = (valid && p.smooth_k) ? load8_raw<T>(kp + tok * p.k_sn, c0, p.d, p.vec16)
-                                    : make_uint4(0, 0, 0, 0);
+      raw[r] = t < t1 ? load8_raw<T>(base + (int64_t)(s.tok0_k + t) * sn, c0, p.d, p.vec16)
+                      : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
       if (t0 + rg + RG * r >= t1) continue;
-      float vx[8], kx[8];
-      unpack8<T>(vr[r], vx);
-      unpack8<T>(kr[r], kx);
+      float x[8];
+      unpack8<T>(raw[r], x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (p.smooth_k) {
-          range_bad |= fabsf(kx[i]) >= lim;
-          ks[i] += __float2ll_rz(kx[i] * 16777216.0f);
+        if (want_sum) {
+          range_bad |= fabsf(x[i]) >= lim;
+          exact &= fixed_split_exact<T>(x[i]);
+          int h, l;
+          fixed_split(x[i], h, l);
+          hi[i] += h;
+          lo[i] += l;
         }
-        if (p.smooth_v) {
-          range_bad |= fabsf(vx[i]) >= lim;
-          vs[i] += __float2ll_rz(vx[i] * 16777216.0f);
+        if (KIND == 1) {
+          mn[i] = fminf(mn[i], x[i]);
+          mx[i] = fmaxf(mx[i], x[i]);
         }
-        vmn[i] = fminf(vmn[i], vx[i]);
-        vmx[i] = fmaxf(vmx[i], vx[i]);
       }
     }
   }
   if (range_bad) record_error(p.err, kDevRange);
+  long long sum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sum[i] = (static_cast<long long>(hi[i]) << 20) + lo[i];
+  if (!std::is_same<T, __half>::value && want_sum && !__all_sync(0xffffffffu, exact)) {
+    // a bf16 value below 2^-17 or above 2^18 in this warp: exact int64 conversion instead
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum[i] = 0;
+    if (active) {
+      for (int r = 0; r < kRows; ++r) {
+        const int t = t0 + rg + RG * r;
+        if (t >= t1) continue;
+        float x[8];
+        unpack8<T>(load8_raw<T>(base + (int64_t)(s.tok0_k + t) * sn, c0, p.d, p.vec16), x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum[i] += __float2ll_rz(x[i] * 16777216.0f);
+      }
+    }
+  }
   // reduce the row groups that share a warp, then the 8 warps through shared memory
 #pragma unroll
   for (int off = TPR; off < 32; off <<= 1) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], off);
-      vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], off);
-      vmn[i] = fminf(vmn[i], __shfl_xor_sync(0xffffffffu, vmn[i], off));
-      vmx[i] = fmaxf(vmx[i], __shfl_xor_sync(0xffffffffu, vmx[i], off));
+      if (want_sum) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], off);
+      if (KIND == 1) {
+        mn[i] = fminf(mn[i], __shfl_xor_sync(0xffffffffu, mn[i], off));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
+      }
     }
   }
   __shared__ long long red_s[8][128];
   __shared__ float red_f[8][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t sidx = ((int64_t)b * p.hkv + hk) * p.d;
-  // pass 1: K sums
-  if (lane < TPR) {
+  if (want_sum) {
+    if (lane < TPR) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = ks[i];
+      for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = sum[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < p.d) {
+      long long acc = 0;
+      for (int w = 0; w < 8; ++w) acc += red_s[w][threadIdx.x];
+      atomicAdd(reinterpret_cast<unsigned long long*>(KIND == 0 ? &p.ksum[sidx + threadIdx.x]
+                                                                 : &p.vsum[sidx + threadIdx.x]),
+                static_cast<unsigned long long>(acc));
+    }
   }
-  __syncthreads();
-  if (p.smooth_k && threadIdx.x < p.d) {
-    long long acc = 0;
-    for (int w = 0; w < 8; ++w) acc += red_s[w][threadIdx.x];
-    atomicAdd(reinterpret_cast<unsigned long long*>(&p.ksum[sidx + threadIdx.x]),
-              static_cast<unsigned long long>(acc));
-  }
-  __syncthreads();
-  // pass 2: V sums
-  if (lane < TPR) {
+  if (KIND == 1) {
+    if (lane < TPR) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red_s[warp][c0 + i] = vs[i];
-  }
-  __syncthreads();
-  if (p.smooth_v && threadIdx.x < p.d) {
-    long long acc = 0;
-    for (int w = 0; w < 8; ++w) acc += red_s[w][threadIdx.x];
-    atomicAdd(reinterpret_cast<unsigned long long*>(&p.vsum[sidx + threadIdx.x]),
-              static_cast<unsigned long long>(acc));
-  }
-  // pass 3: V min
-  if (lane < TPR) {
+      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = mn[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < p.d) {
+      float m = red_f[0][threadIdx.x];
+      for (int w = 1; w < 8; ++w) m = fminf(m, red_f[w][threadIdx.x]);
+      atomicMin(&p.vmin[sidx + threadIdx.x], float_to_ordered(m));
+    }
+    __syncthreads();
+    if (lane < TPR) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmn[i];
-  }
-  __syncthreads();
-  if (threadIdx.x < p.d) {
-    float m = red_f[0][threadIdx.x];
-    for (int w = 1; w < 8; ++w) m = fminf(m, red_f[w][threadIdx.x]);
-    atomicMin(&p.vmin[sidx + threadIdx.x], float_to_ordered(m));
-  }
-  __syncthreads();
-  // pass 4: V max
-  if (lane < TPR) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = vmx[i];
-  }
-  __syncthreads();
-  if (threadIdx.x < p.d) {
-    float m = red_f[0][threadIdx.x];
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, red_f[w][threadIdx.x]);
-    atomicMax(&p.vmax[sidx + threadIdx.x], float_to_ordered(m));
+      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = mx[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < p.d) {
+      float m = red_f[0][threadIdx.x];
+      for (int w = 1; w < 8; ++w) m = fmaxf(m, red_f[w][threadIdx.x]);
+      atomicMax(&p.vmax[sidx + threadIdx.x], float_to_ordered(m));
+    }
   }
 }
 
@@ -239,7 +251,7 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //      [channel][token] so that P.V reads V^T tiles K-major.
 // Rows past the sequence end up to the stored tile end are written as zeros.
 template <typename T, int kind, int TPR>
-__global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
+__global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
   constexpr int RG = 256 / TPR;      // row groups
   constexpr int RPT = kTileRows / RG;  // rows per thread
   const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -388,12 +400,15 @@ __global__ void __launch_bounds__(256, 3) quant_kernel(Problem p) {
     const float rc = grcp[rr / gs];
     float x[8];
     row_values(i, x);
-    __align__(16) __half hv[8];
+    __align__(16) __half2 hv[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      int c = __float2int_rn(__fmul_rn(x[j], rc));
-      c = max(-127, min(127, c));
-      hv[j] = __int2half_rn(c);
+    for (int j = 0; j < 8; j += 2) {
+      // rint_even(fl32(x * r)) via the rounding constant (|x * r| <= 127.00002 < 2^22)
+      float c0 = __fsub_rn(__fadd_rn(__fmul_rn(x[j], rc), kRoundMagic), kRoundMagic);
+      float c1 = __fsub_rn(__fadd_rn(__fmul_rn(x[j + 1], rc), kRoundMagic), kRoundMagic);
+      c0 = fminf(fmaxf(c0, -127.0f), 127.0f);
+      c1 = fminf(fmaxf(c1, -127.0f), 127.0f);
+      hv[j / 2] = __floats2half2_rn(c0, c1);  // exact: integers of magnitude <= 127
     }
     if (c0 < dp && r < stored)
       *reinterpret_cast<uint4*>(codes + (plane * rows_pp + row0 + r) * dp + c0) =
@@ -452,12 +467,18 @@ cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st) {
 
 template <typename T>
 static void launch_kv_stats_t(const Problem& p, dim3 grid, cudaStream_t st) {
-  if (p.dp == 64) kv_stats_kernel<T, 8><<<grid, 256, 0, st>>>(p);
-  else kv_stats_kernel<T, 16><<<grid, 256, 0, st>>>(p);
+  if (p.dp == 64) {
+    if (p.smooth_k) kv_stats_kernel<T, 8, 0><<<grid, 256, 0, st>>>(p);
+    kv_stats_kernel<T, 8, 1><<<grid, 256, 0, st>>>(p);
+  } else {
+    if (p.smooth_k) kv_stats_kernel<T, 16, 0><<<grid, 256, 0, st>>>(p);
+    kv_stats_kernel<T, 16, 1><<<grid, 256, 0, st>>>(p);
+  }
 }
 
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
-  const dim3 grid((max_len_k + kStatsChunk - 1) / kStatsChunk, p.hkv, p.batch);
+  const int chunk = stats_chunk(p.dp);
+  const dim3 grid((max_len_k + chunk - 1) / chunk, p.hkv, p.batch);
   if (p.dtype == 0) launch_kv_stats_t<__half>(p, grid, st);
   else launch_kv_stats_t<__nv_bfloat16>(p, grid, st);
   return cudaGetLastError();

@@ -25,6 +25,8 @@ Parity status per function (see the pins in ``tests/test_oracle_*.py``):
                                           smooth_k invariance; cosine vs fp64)
   attention fp16+fp32 accumulation       parity unpinned beyond the bypass/closed forms: the
                                           in-tile rounding order is a reading, not a definition
+  merge.merge_partials                   pinned (chunked fp64 attention merges to the unchunked
+                                          result; empty parts; single part; order invariance)
 """
 
-from . import fp8, quant, attention  # noqa: F401
+from . import fp8, quant, attention, merge  # noqa: F401

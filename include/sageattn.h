@@ -155,6 +155,24 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
                      int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Composition of partial results over disjoint key sets (pwwt.cn "SageAttention deployment
+ * pitfalls guide" §4.1: return_lse exists for Ring Attention and similar schemes, which attend
+ * to chunks of the keys separately). For every (b, h, n) row:
+ *   lse = ln sum_i exp(lse_i),   out = sum_i exp(lse_i - lse) * out_i
+ * computed in fp32 and rounded once to `dtype`.
+ *   outs[0..n_parts): device tensors in `tensor_layout` (as sage_attn's out, dtype `dtype`);
+ *   lses[0..n_parts): device float [B, H, N] contiguous (as sage_attn writes them);
+ *   out: device tensor of the same shape (may alias outs[0]); lse_out: device float
+ *   [B, H, N] or NULL. The pointer arrays themselves are host memory.
+ * A part whose lse is -inf contributes nothing; a row no part sees gets out = 0 and
+ * lse = -inf. 1 <= n_parts <= SAGE_MAX_MERGE_PARTS. Errors: SAGE_ERR_INVALID_ARG (counts,
+ * null pointers, layout), SAGE_ERR_DTYPE, SAGE_ERR_HEAD_DIM, SAGE_ERR_STRIDE (pointer not
+ * 2-byte aligned, negative stride), SAGE_ERR_CUDA. Nothing is launched for an empty problem. */
+#define SAGE_MAX_MERGE_PARTS 16
+int sage_merge_partials(const sage_tensor* outs, const float* const* lses, int n_parts,
+                        const sage_tensor* out, float* lse_out, int batch, int heads,
+                        int seqlen, int head_dim, int dtype, int tensor_layout, void* stream);
+
 /* Human-readable name of a sage_status. Never NULL. */
 const char* sage_status_string(int status);
 

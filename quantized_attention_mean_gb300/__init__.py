@@ -8,7 +8,8 @@ memory and streams; every step of the computation runs in the library's CUDA ker
                     smooth_k=True, smooth_v=False)
 
 mirrors the ``sageattn`` API (pwwt.cn "SageAttention deployment pitfalls guide" §4.1, §4.2);
-``sage_attn_varlen`` mirrors ``sageattn_varlen``.
+``sage_attn_varlen`` mirrors ``sageattn_varlen``; ``merge_partials`` combines results over
+disjoint key chunks through their log-sum-exp (ring / context-parallel composition).
 """
 
 import ctypes
@@ -149,6 +150,39 @@ def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     _check(st, "sage_attn_varlen")
     return (out, lse) if return_lse else out
+
+
+def merge_partials(outs, lses, tensor_layout="HND", out=None, lse=None, stream=None):
+    """Combines attention results computed over disjoint key sets (each from ``sage_attn``
+    with ``return_lse=True``): lse = ln sum_i exp(lse_i), out = sum_i exp(lse_i - lse) out_i.
+    outs: tensors of one shape/layout/dtype ([B, H, N, d] HND or [B, N, H, d] NHD); lses:
+    fp32 [B, H, N]. Returns (out, lse)."""
+    lib = _lib.load()
+    if len(outs) != len(lses) or not outs:
+        raise ValueError("one lse per partial output, at least one part")
+    o0 = outs[0]
+    if o0.dtype not in DTYPE or any(o.dtype != o0.dtype or o.shape != o0.shape for o in outs):
+        raise TypeError("partial outputs must share one shape and a float16/bfloat16 dtype")
+    if tensor_layout == "HND":
+        B, H, N, d = o0.shape
+    else:
+        B, N, H, d = o0.shape
+    for l in lses:
+        if l.dtype != torch.float32 or tuple(l.shape) != (B, H, N) or not l.is_contiguous():
+            raise ValueError("each lse must be a contiguous float32 [B, H, N] tensor")
+    if out is None:
+        out = torch.empty_like(o0)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o0.device)
+    views = (SageTensor * len(outs))(*[_tensor(o) for o in outs])
+    ptrs = (ctypes.c_void_p * len(lses))(*[l.data_ptr() for l in lses])
+    with torch.cuda.device(o0.device):
+        st = lib.sage_merge_partials(ctypes.cast(views, ctypes.c_void_p), ctypes.cast(ptrs, ctypes.c_void_p),
+                                     len(outs), ctypes.byref(_tensor(out)),
+                                     ctypes.c_void_p(lse.data_ptr()), B, H, N, d, DTYPE[o0.dtype],
+                                     LAYOUT[tensor_layout], _stream_ptr(stream))
+    _check(st, "sage_merge_partials")
+    return out, lse
 
 
 def read_device_status(workspace, stream=None):

@@ -44,16 +44,20 @@ struct AttnCfg {
   static constexpr int kPTileBytes = kTileRows * kTileKeys;     // E4M3
   static constexpr int kKStages = DP == 128 ? 2 : 3;
   static constexpr int kVStages = DP == 128 ? 2 : 3;
+  // P buffers per query tile: with two, the softmax writes P_j while P.V of tile j - 1 may
+  // still be reading P_{j-1} (shared memory allows it for DP = 64 only)
+  static constexpr int kPBufs = DP == 64 ? 2 : 1;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBufs * kPTileBytes;
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
   static constexpr int kSmem = (kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024);
+  static_assert(kBytes + 1024 <= 232448, "shared memory budget");
 };
 
 // Instruction descriptors: M = 128 rows, fp32 accumulate, K-major operands.
@@ -301,9 +305,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&s_full[x]);
       };
-      auto issue_pv = [&](int x, int sv, bool first) {
+      auto issue_pv = [&](int x, int sv, int buf, bool first) {
         const uint32_t d_o = tmem + (x ? 384u : 256u);
-        const uint64_t px = dp + static_cast<uint64_t>((x * C::kPTileBytes) >> 4);
+        const uint64_t px =
+            dp + static_cast<uint64_t>(((x * C::kPBufs + buf) * C::kPTileBytes) >> 4);
         const uint64_t vst = dv + static_cast<uint64_t>((sv * C::kVTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kTileKeys / 32; ++k)
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (x == 0) ok = mbar_wait(&v_full[sv], (j / C::kVStages) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(x, sv, j == 0);
+          issue_pv(x, sv, j % C::kPBufs, j == 0);
           trace(p, tr, 2, j, 4 * x + 3);
         }
         if (!ok) break;
@@ -361,7 +366,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x == 0 ? 0u : 128u);
     const uint32_t tO = tmem + lane_base + (x == 0 ? 256u : 384u);
-    uint8_t* my_p = sP + x * C::kPTileBytes + r * 128;
+    uint8_t* const p_row = sP + x * C::kPBufs * C::kPTileBytes + r * 128;  // + buffer offset
     const int xrows = x == 0 ? rows_a : rows_b;
     const bool active_tile = x == 0 || has_b;
     const int i = q_start + x * kTileRows + r;  // query row within the sequence
@@ -436,12 +441,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
         const float bias = log2_sigma - m_use;
-        // the P buffer is free once the previous P.V of this tile has completed
-        if (j > 0) {
+        // with one P buffer it is free once P.V of tile j - 1 has completed; with two, P.V of
+        // tile j - 2 (its previous reader) completed before this row's rescale wait of tile
+        // j - 1 below
+        if (C::kPBufs == 1 && j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
         }
+        uint8_t* const my_p = p_row + (j % C::kPBufs) * C::kPTileBytes;
         trace(p, trs, x, j, 4);
         // P~ = e4m3(2^(x - m) * sigma) written 16 keys (one 16-byte chunk, 128-byte swizzle)
         // at a time; the row sum uses four independent accumulator pairs
@@ -490,7 +498,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&p_full[x]);
         trace(p, trs, x, j, 5);
         // rescale this warp's O rows for the grown max while the next scores are computed;
-        // P_j(x) V_j is issued only after o_ready
+        // P_j(x) V_j is issued only after o_ready. O holds the sum up to tile j - 1 once P.V
+        // of tile j - 1 is complete.
+        if (C::kPBufs > 1 && j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
         if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
 #pragma unroll
           for (int c2 = 0; c2 < DP / 64; ++c2) {

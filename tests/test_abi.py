@@ -87,3 +87,30 @@ def test_host_validation_statuses(lib):
 def test_null_tensor_is_invalid(lib):
     assert lib.sage_attn(None, None, None, None, None, 1, 2, 2, 8, 8, 64, 0, 0, 0, 0.0, 0, 1, 0,
                          1, 0, None, 0, None) == 1
+
+
+def test_merge_partials_host_validation(lib):
+    from quantized_attention_mean_gb300._lib import SageTensor
+    fake = 0x10000  # never dereferenced: validation fails before any launch
+    t = SageTensor(fake, (ctypes.c_int64 * 3)(8 * 4 * 64, 4 * 64, 64))
+    views = (SageTensor * 2)(t, t)
+    lses = (ctypes.c_void_p * 2)(fake, fake)
+    args = dict(outs=ctypes.cast(views, ctypes.c_void_p), lses=ctypes.cast(lses, ctypes.c_void_p),
+                n=2, out=ctypes.byref(t), lse=ctypes.c_void_p(fake), B=1, H=2, N=3, d=64, dtype=0,
+                layout=0)
+
+    def call(**over):
+        a = dict(args, **over)
+        return lib.sage_merge_partials(a["outs"], a["lses"], a["n"], a["out"], a["lse"], a["B"],
+                                       a["H"], a["N"], a["d"], a["dtype"], a["layout"], None)
+    assert call(n=0) == 1
+    assert call(n=17) == 1
+    assert call(layout=5) == 1
+    assert call(dtype=9) == 3
+    assert call(d=129) == 2
+    assert call(d=0) == 2
+    assert call(B=0) == 0            # empty problem: nothing launched
+    bad = SageTensor(fake + 1, (ctypes.c_int64 * 3)(64, 64, 64))
+    assert call(out=ctypes.byref(bad)) == 4
+    neg = SageTensor(fake, (ctypes.c_int64 * 3)(-64, 64, 64))
+    assert call(out=ctypes.byref(neg)) == 4

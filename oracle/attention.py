@@ -22,6 +22,11 @@ The steps, in the order the method applies them, per (batch, query head):
   9. O = acc · s_v / (σ_P · l) + v̄, rounded once to the output dtype
  10. LSE = m + ln l + sm_scale · (q · k̄)   (natural log; undoes the smooth_k shift)
 Steps 5-10 use library matmuls on exact integer or float64 operands only.
+
+FP16 P·V variant (pv="fp16"; the guide's §5.3 / §5.4 INT8-QK + FP16-PV kernel, its quality
+fallback with FP8 turned off): step 3 keeps V' as fp16 (RNE) instead of E4M3 with a scale,
+step 7 rounds P to fp16 with σ_P = 1, and step 9 has no V scale. Steps 4-6, 8 and 10 are
+unchanged (the fp16+fp32 mode keeps its per-tile fp16 rounding).
 """
 
 import numpy as np
@@ -73,8 +78,8 @@ def to_bf16(x):
 
 
 # --------------------------------------------------------------------------- stages 1-3
-def quantize_kv_head(k, v, gran, smooth_k, smooth_v):
-    """Stages 1-3 for one KV head: k, v float32 [Nk, d]."""
+def quantize_kv_head(k, v, gran, smooth_k, smooth_v, pv="fp8"):
+    """Stages 1-3 for one KV head: k, v float32 [Nk, d]. pv="fp16" keeps V' in fp16."""
     k = np.asarray(k, np.float32)
     v = np.asarray(v, np.float32)
     d = k.shape[1]
@@ -83,8 +88,14 @@ def quantize_kv_head(k, v, gran, smooth_k, smooth_v):
     ks = smooth(k, kbar)
     vs = smooth(v, vbar)
     k8, sk = int8_group_quant(ks, K_GROUP[gran])
+    if pv == "fp16":
+        return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk,
+                    v16=to_fp16(vs), pv="fp16")
+    if pv != "fp8":
+        raise ValueError("pv must be 'fp8' or 'fp16'")
     v8, sv = fp8_channel_quant(vs)
-    return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk, v8=v8, sv=sv)
+    return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk, v8=v8, sv=sv,
+                pv="fp8")
 
 
 def quantize_q_head(q, gran):
@@ -105,21 +116,30 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
     q: float32 [Nq, d] (original values, used for Q quantisation and the LSE term);
     kvq: output of quantize_kv_head; rows: query rows to compute (default all).
     bypass_quant replaces every code by the value it encodes (scales 1, P unrounded):
-    the result must then equal exact attention, which pins the non-quantising steps.
+    the result must then equal exact attention, which pins the non-quantising steps;
+    bypass_quant="qk" bypasses only the Q/K codes (P and V keep their P·V format).
     Returns dict(o=float64 [R, d] before output rounding, lse=float64 [R]).
     """
     q = np.asarray(q, np.float32)
     nq, d = q.shape
     nk = kvq["k8"].shape[0]
     rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
-    sig = sigma_p(accum)
-    if bypass_quant:
+    pv16 = kvq.get("pv") == "fp16"
+    sig = 1.0 if pv16 else sigma_p(accum)
+    if accum == ACC_FP16:
+        sigma_p(accum)  # raises: pure fp16 accumulation is not supported
+    if bypass_quant is True:
         qv = q.astype(np.float64)
         sq_row = np.ones(nq)
         kv = kvq["k_smoothed"].astype(np.float64)
         sk_key = np.ones(nk)
         vd = kvq["v_smoothed"].astype(np.float64)
         sv = np.ones(d)
+    elif bypass_quant == "qk":
+        qv = q.astype(np.float64)
+        sq_row = np.ones(nq)
+        kv = kvq["k_smoothed"].astype(np.float64)
+        sk_key = np.ones(nk)
     else:
         if qq is None:
             qq = quantize_q_head(q, gran)
@@ -127,8 +147,13 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
         sq_row = qq["sq"].astype(np.float64)[np.arange(nq) // Q_GROUP[gran]]
         kv = kvq["k8"].astype(np.float64)
         sk_key = kvq["sk"].astype(np.float64)[np.arange(nk) // K_GROUP[gran]]
-        vd = e4m3_decode(kvq["v8"])
-        sv = kvq["sv"].astype(np.float64)
+    if bypass_quant is not True:
+        if pv16:
+            vd = kvq["v16"].astype(np.float64)
+            sv = np.ones(d)
+        else:
+            vd = e4m3_decode(kvq["v8"])
+            sv = kvq["sv"].astype(np.float64)
     vbar = kvq["vbar"].astype(np.float64)
     kbar = kvq["kbar"].astype(np.float64)
 
@@ -144,11 +169,13 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
         m = t.max(axis=1)                                  # step 6
         p = np.exp(t - m[:, None])
         l = p.sum(axis=1)
-        if bypass_quant:                                   # step 7
+        if bypass_quant is True:                           # step 7
             pq = p * sig
+        elif pv16:
+            pq = to_fp16(p)
         else:
             pq = e4m3_decode(e4m3_encode(p * sig))
-        if accum == ACC_FP16_FP32 and not bypass_quant:   # step 8
+        if accum == ACC_FP16_FP32 and bypass_quant is not True:   # step 8
             acc = np.zeros((len(r), d))
             for k0 in range(0, nk, PV_TILE):
                 acc += to_fp16(pq[:, k0:k0 + PV_TILE] @ vd[k0:k0 + PV_TILE])
@@ -169,7 +196,7 @@ def _check_args(hq, hkv, d, accum):
 
 def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WARP,
                    accum=ACC_FP32, smooth_k=True, smooth_v=False, heads=None, rows=None,
-                   bypass_quant=False):
+                   bypass_quant=False, pv="fp8"):
     """Dense forward on canonical float32 arrays q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d].
 
     heads: optional list of (b, hq) pairs to compute (default all); rows: optional query
@@ -196,7 +223,7 @@ def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WAR
         key = (b, h // group)
         if key not in kvcache:
             kvcache[key] = quantize_kv_head(k[b, h // group], v[b, h // group], gran,
-                                            smooth_k, smooth_v)
+                                            smooth_k, smooth_v, pv=pv)
         qcache[(b, h)] = quantize_q_head(q[b, h], gran)
         res = attend_head(q[b, h], kvcache[key], gran=gran, sm_scale=sm_scale,
                           is_causal=is_causal, accum=accum, rows=rows, qq=qcache[(b, h)],

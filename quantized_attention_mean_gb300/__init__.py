@@ -185,6 +185,35 @@ def merge_partials(outs, lses, tensor_layout="HND", out=None, lse=None, stream=N
     return out, lse
 
 
+def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.0,
+                                 is_causal=False, scale=None, enable_gqa=False, **sage_kwargs):
+    """Stand-in for ``torch.nn.functional.scaled_dot_product_attention`` on the quantized path
+    (the pages present the method as a replacement for that call; pwwt.cn "SageAttention
+    deployment pitfalls guide" §4.1, §5.1: a one-line replacement of that function; masks
+    other than causal are not supported).
+
+    query [B, H, L, d] or [H, L, d]; key / value [B, Hkv, S, d] or [Hkv, S, d] (HND), fp16 or
+    bf16, head_dim <= 128. ``is_causal`` masks key j for query i when j > i (top-left, as
+    torch). ``scale`` defaults to 1/sqrt(d). Key/value heads may divide the query heads
+    (grouped-query attention) whatever ``enable_gqa`` says. Arbitrary masks and dropout are
+    not supported by the method and raise NotImplementedError. Extra keyword arguments go to
+    ``sage_attn`` (qk_quant_gran, pv_accum_dtype, smooth_k, smooth_v)."""
+    if attn_mask is not None:
+        raise NotImplementedError("attn_mask: the quantized kernel supports only causal or no masking")
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout_p must be 0")
+    if query.dim() not in (3, 4) or key.dim() != query.dim() or value.dim() != query.dim():
+        raise ValueError("expected [B, H, N, d] or [H, N, d] tensors")
+    squeeze = query.dim() == 3
+    if squeeze:
+        query, key, value = query.unsqueeze(0), key.unsqueeze(0), value.unsqueeze(0)
+    if key.shape[1] == 0 or query.shape[1] % key.shape[1] != 0:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (query, key, value))
+    out = sage_attn(q, k, v, tensor_layout="HND", is_causal=is_causal, sm_scale=scale, **sage_kwargs)
+    return out.squeeze(0) if squeeze else out
+
+
 def read_device_status(workspace, stream=None):
     return _lib.load().sage_read_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream_ptr(stream))
 

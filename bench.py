@@ -29,6 +29,11 @@ METRIC = "quantized attention TOPS (4·B·H·Nq·Nk·d/s) at 1 GB300; % of INT8/
 UNIT = "TOPS"
 L2_BYTES = 129 * 2**20
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, from the ncu
+# capture summarised in profiles/ (same kernel source); None where no capture exists. Must be
+# cleared whenever the attention kernel changes.
+ATTN_DRAM_BYTES = {"sdpa4k": 42_171_136}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -287,7 +292,7 @@ def run_ours(args, w):
     achieved = ops / (attn_ms / 1e3) / 1e12
     fp8_peak = 2.0 * pk["bf16"]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": None,
+                "frac": achieved / fp8_peak, "traffic": ATTN_DRAM_BYTES.get(w.name),
                 "kernel": "attn_kernel<128> (fused QK^T/softmax/PV)",
                 "peak_source": f"{pk['src']}: dense FP8 = 2 x bf16 burst {pk['bf16']} TFLOP/s",
                 "route_ceiling_frac": 2.0 / 3.0,

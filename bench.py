@@ -51,7 +51,8 @@ def describe(w):
     lay = f"{w.B}x{w.Hq}" + (f"/{w.Hkv}" if w.Hkv != w.Hq else "")
     return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq={w.Nq} Nk={w.Nk} d={w.d} {w.dtype} "
             f"{w.layout} causal={int(w.is_causal)} {w.gran} smooth_k={int(w.smooth_k)} "
-            f"smooth_v={int(w.smooth_v)} pv_accum={w.accum} lse={int(w.return_lse)} ({lay})")
+            f"smooth_v={int(w.smooth_v)} pv_accum={w.accum} lse={int(w.return_lse)} "
+            f"pv={w.extra.get('pv', 'fp8')} ({lay})")
 
 
 def peaks():
@@ -164,7 +165,7 @@ def oracle_sample(w, rows, seed=0):
     qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
     g = GRAN[w.gran]
     t0 = time.perf_counter()
-    kvq = quantize_kv_head(kn[0, 0], vn[0, 0], g, w.smooth_k, w.smooth_v)
+    kvq = quantize_kv_head(kn[0, 0], vn[0, 0], g, w.smooth_k, w.smooth_v, pv=w.extra.get("pv", "fp8"))
     qq = quantize_q_head(qn[0, 0], g)
     attend_head(qn[0, 0], kvq, gran=g, sm_scale=default_sm_scale(w.d), is_causal=w.is_causal,
                 accum=ACC[w.accum], rows=np.arange(rows), qq=qq)
@@ -250,13 +251,15 @@ def run_ours(args, w):
     kw = dict(is_causal=w.is_causal, return_lse=w.return_lse, qk_quant_gran=w.gran,
               pv_accum_dtype=w.accum, smooth_k=w.smooth_k, smooth_v=w.smooth_v)
     stream = torch.cuda.current_stream()
+    # the FP16 P·V variant has its own entry point
+    dense_call = qa.sage_attn_qk_int8_pv_fp16 if w.extra.get("pv") == "fp16" else qa.sage_attn
 
     def step(i):
         q, k, v, out, lse, ws, cu = sets[i % nsets]
         if w.varlen:
             qa.sage_attn_varlen(q, k, v, cu, cu, max(lens), max(lens), out=out, lse=lse, workspace=ws, **kw)
         else:
-            qa.sage_attn(q, k, v, tensor_layout=w.layout, out=out, lse=lse, workspace=ws, **kw)
+            dense_call(q, k, v, tensor_layout=w.layout, out=out, lse=lse, workspace=ws, **kw)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -314,7 +317,7 @@ def run_ours(args, w):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            qa.sage_attn(dq, dk, dv, out=dout, workspace=wse, **{**kw, "return_lse": False})
+            dense_call(dq, dk, dv, out=dout, workspace=wse, **{**kw, "return_lse": False})
             ho.copy_(dout, non_blocking=True)
 
         for _ in range(3):
@@ -345,7 +348,7 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8 QK (exact, fp16 carrier) + e4m3 PV, fp32 softmax",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 QK (exact, fp16 carrier) + " + ("fp16" if w.extra.get("pv") == "fp16" else "e4m3") + " PV, fp32 softmax",
             "data": "synthetic",
             "config": {"workload": describe(w), "parallelism": f"replicas x{ws_n} (independent heads/batches)",
                        "l2": f"inputs rotate over {nsets} resident sets ({nsets * (per_set + wsb) / 2**20:.0f} MiB > L2 129 MiB)"},

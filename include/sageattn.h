@@ -106,6 +106,20 @@ int sage_attn(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
               int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
               size_t workspace_bytes, void* stream);
 
+/* FP16 P·V variant (pwwt.cn "SageAttention deployment pitfalls guide" §5.3–§5.4: the INT8-QK
+ * + FP16-PV kernel, the quality fallback with FP8 turned off): as sage_attn, with the same
+ * arguments, workspace size and errors, except that V' = V - v̄ is kept in fp16 (no per-channel
+ * scale) and P = 2^(t - m) is rounded to fp16 (σ_P = 1); both P·V operands are fp16 on the
+ * tensor cores (kind::f16) with fp32 accumulation. pv_accum_dtype: SAGE_ACC_FP32,
+ * SAGE_ACC_FP32_FP32 or SAGE_ACC_FP16_FP32 (all accumulate in fp32); SAGE_ACC_FP16 returns
+ * SAGE_ERR_UNSUPPORTED. |V - v̄| beyond the fp16 range becomes ±inf. */
+int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                              const sage_tensor* out, float* lse, int batch, int heads_q,
+                              int heads_kv, int seqlen_q, int seqlen_k, int head_dim, int dtype,
+                              int tensor_layout, int is_causal, float sm_scale, int return_lse,
+                              int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /* Capacity of the scratch array built into the library for sage_attn_no_alloc. */
 #define SAGE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 

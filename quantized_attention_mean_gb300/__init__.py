@@ -83,7 +83,7 @@ def _dims(q, k, layout):
 
 def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, return_lse=False,
               qk_quant_gran="per_warp", pv_accum_dtype="fp32", smooth_k=True, smooth_v=False,
-              out=None, lse=None, workspace=None, stream=None, _debug_scores=None):
+              out=None, lse=None, workspace=None, stream=None, _debug_scores=None, _pv16=False):
     """Quantized attention forward. q: [B, Hq, Nq, d] (HND) or [B, Nq, Hq, d] (NHD);
     k, v: [B, Hkv, Nk, d] / [B, Nk, Hkv, d]; fp16 or bf16 on one CUDA device.
     Returns out (same shape/layout/dtype as q), plus lse [B, Hq, Nq] fp32 if return_lse."""
@@ -108,13 +108,28 @@ def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, retu
             int(bool(smooth_k)), int(bool(smooth_v)), ctypes.c_void_p(workspace.data_ptr()),
             workspace.numel()]
     with torch.cuda.device(q.device):
-        if _debug_scores is None:
+        if _pv16:
+            st = lib.sage_attn_qk_int8_pv_fp16(*args, _stream_ptr(stream))
+        elif _debug_scores is None:
             st = lib.sage_attn(*args, _stream_ptr(stream))
         else:
             st = lib.sage_attn_debug_scores(*args, ctypes.c_void_p(_debug_scores.data_ptr()),
                                             _stream_ptr(stream))
     _check(st, "sage_attn")
     return (out, lse) if return_lse else out
+
+
+def sage_attn_qk_int8_pv_fp16(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None,
+                              return_lse=False, qk_quant_gran="per_warp", pv_accum_dtype="fp32",
+                              smooth_k=True, smooth_v=False, out=None, lse=None, workspace=None,
+                              stream=None):
+    """The FP16 P·V variant (INT8 Q/K; P and V' in fp16 on the tensor cores), mirroring the
+    pages' ``sageattn_qk_int8_pv_fp16_cuda`` quality fallback. Arguments and results as
+    ``sage_attn``."""
+    return sage_attn(q, k, v, tensor_layout=tensor_layout, is_causal=is_causal, sm_scale=sm_scale,
+                     return_lse=return_lse, qk_quant_gran=qk_quant_gran,
+                     pv_accum_dtype=pv_accum_dtype, smooth_k=smooth_k, smooth_v=smooth_v, out=out,
+                     lse=lse, workspace=workspace, stream=stream, _pv16=True)
 
 
 def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,

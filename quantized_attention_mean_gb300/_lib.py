@@ -28,6 +28,8 @@ SIGNATURES = {
     "sage_attn_workspace_size": (c_size_t, [c_int] * 7),
     "sage_attn": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float] + [c_int] * 5
                   + [c_void_p, c_size_t, c_void_p]),
+    "sage_attn_qk_int8_pv_fp16": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float]
+                                  + [c_int] * 5 + [c_void_p, c_size_t, c_void_p]),
     "sage_attn_no_alloc": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float] + [c_int] * 5
                            + [c_void_p]),
     "sage_attn_varlen_workspace_size": (c_size_t, [c_int] * 7),

@@ -67,7 +67,8 @@ bool make_layout(bool varlen, int batch, int hq, int hkv, int64_t lq, int64_t lk
   L->off_vrcp = take(4 * L->n_stats);
   L->off_qc = take(2 * (size_t)L->planes_q * L->q_rows * L->dp);
   L->off_kc = take(2 * (size_t)L->planes_kv * L->k_rows * L->dp);
-  L->off_vt = take((size_t)L->planes_kv * L->dp * L->vt_pitch);
+  // V^T: E4M3 bytes, or fp16 for the FP16 P·V variant (two bytes reserved per element)
+  L->off_vt = take((size_t)L->planes_kv * L->dp * L->vt_pitch * 2);
   L->off_sq = take(4 * (size_t)L->planes_q * L->sq_pp);
   L->off_sk = take(4 * (size_t)L->planes_kv * L->sk_pp);
   L->off_qkc = take(4 * (size_t)L->planes_q * L->q_rows);
@@ -235,9 +236,12 @@ int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cuda
                      dp * 2, dp * 2 * L.q_rows, 64, 128) &&
             make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.kc, dp, L.k_rows, L.planes_kv,
                      dp * 2, dp * 2 * L.k_rows, 64, 128) &&
-            make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.vt,
-                     p.varlen ? L.k_rows : static_cast<uint64_t>(p.nk), dp, L.planes_kv,
-                     L.vt_pitch, L.vt_pitch * dp, 128, L.dp);
+            (p.pv16 ? make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.vt,
+                               p.varlen ? L.k_rows : static_cast<uint64_t>(p.nk), dp, L.planes_kv,
+                               L.vt_pitch * 2, L.vt_pitch * 2 * dp, 64, L.dp)
+                    : make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.vt,
+                               p.varlen ? L.k_rows : static_cast<uint64_t>(p.nk), dp, L.planes_kv,
+                               L.vt_pitch, L.vt_pitch * dp, 128, L.dp));
   if (!ok) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   StageEvents* ev = prof_next();
   auto mark = [&](int i) { if (ev) cudaEventRecord(ev->e[i], st); };
@@ -261,7 +265,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                const sage_tensor* out, float* lse, int batch, int hq, int hkv, int nq, int nk,
                int d, int dtype, int layout, int is_causal, float sm_scale, int return_lse,
                int gran, int acc, int smooth_k, int smooth_v, void* ws, size_t ws_bytes,
-               int32_t* dbg_scores, void* stream) {
+               int32_t* dbg_scores, void* stream, int pv16 = 0) {
   if (!q || !k || !v || !out) return SAGE_ERR_INVALID_ARG;
   const Common c{hq, hkv, d, dtype, is_causal, return_lse, gran, acc, smooth_k, smooth_v, sm_scale};
   int st = check_common(c, lse);
@@ -288,6 +292,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   std::memset(&p, 0, sizeof(p));
   fill_common(p, c);
   p.batch = batch; p.nq = nq; p.nk = nk; p.varlen = 0; p.vec16 = vec16 ? 1 : 0;
+  p.pv16 = pv16;
   // element strides (b, h, n) from the layout's dimension order
   auto bhn = [layout](const sage_tensor* t, int64_t& sb, int64_t& sh, int64_t& sn) {
     sb = t->stride[0];
@@ -331,6 +336,18 @@ int sage_attn(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                     dtype, tensor_layout, is_causal, sm_scale, return_lse, qk_quant_gran,
                     pv_accum_dtype, smooth_k, smooth_v, workspace, workspace_bytes, nullptr,
                     stream);
+}
+
+int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                              const sage_tensor* out, float* lse, int batch, int heads_q,
+                              int heads_kv, int seqlen_q, int seqlen_k, int head_dim, int dtype,
+                              int tensor_layout, int is_causal, float sm_scale, int return_lse,
+                              int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return dense_impl(q, k, v, out, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, head_dim,
+                    dtype, tensor_layout, is_causal, sm_scale, return_lse, qk_quant_gran,
+                    pv_accum_dtype, smooth_k, smooth_v, workspace, workspace_bytes, nullptr,
+                    stream, 1);
 }
 
 int sage_attn_debug_scores(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,

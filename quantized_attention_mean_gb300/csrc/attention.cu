@@ -35,18 +35,19 @@ constexpr int kAttnThreads = 384;
 constexpr uint32_t kRegsSoftmax = 224, kRegsControl = 56;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int DP>
+// PV16: the FP16 P·V variant (P and V' in fp16, P·V on kind::f16); otherwise E4M3 P and V.
+template <int DP, bool PV16 = false>
 struct AttnCfg {
   static constexpr int kChunks = DP / 64;                       // 128-byte K-chunks of a row
   static constexpr int kQTileBytes = kTileRows * DP * 2;        // fp16 codes
   static constexpr int kKTileBytes = kTileKeys * DP * 2;
-  static constexpr int kVTileBytes = DP * kTileKeys;            // E4M3, V^T
-  static constexpr int kPTileBytes = kTileRows * kTileKeys;     // E4M3
+  static constexpr int kVTileBytes = DP * kTileKeys * (PV16 ? 2 : 1);    // V^T, E4M3 or fp16
+  static constexpr int kPTileBytes = kTileRows * kTileKeys * (PV16 ? 2 : 1);  // E4M3 or fp16
   static constexpr int kKStages = DP == 128 ? 2 : 3;
-  static constexpr int kVStages = DP == 128 ? 2 : 3;
+  static constexpr int kVStages = DP == 128 ? (PV16 ? 1 : 2) : 3;
   // P buffers per query tile: with two, the softmax writes P_j while P.V of tile j - 1 may
   // still be reading P_{j-1} (shared memory allows it for DP = 64 only)
-  static constexpr int kPBufs = DP == 64 ? 2 : 1;
+  static constexpr int kPBufs = DP == 64 && !PV16 ? 2 : 1;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
@@ -117,8 +118,34 @@ __device__ __noinline__ float masked_tile_max(uint32_t tS, int limit, Mult8 cg) 
   return tile_max;
 }
 
-// P~ = e4m3(2^(S*c + bias)) for keys [0, limit) (0 beyond), written to the row's swizzled
+// Stores the P values of one 16-key group g of row r (w: E4M3 bytes or fp16 pairs) into the
+// row's P buffer: 128-byte swizzled K-major rows, E4M3 one 16-byte unit per group, fp16 two
+// units per group with 64 keys per 128-row chunk.
+template <bool PV16>
+__device__ __forceinline__ void store_p_group(uint8_t* my_p, int r, int g, const uint32_t (&w)[PV16 ? 8 : 4]) {
+  if constexpr (PV16) {
+    uint8_t* chunk = my_p + (g >> 2) * (kTileRows * 128);
+    const int u0 = (g & 3) * 2;
+    *reinterpret_cast<uint4*>(chunk + ((u0 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+    *reinterpret_cast<uint4*>(my_p + ((g ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+// Two P values in the P buffer's format: E4M3 (bits 0-15 used) or an fp16 pair.
+template <bool PV16>
+__device__ __forceinline__ uint32_t pack_p2(float lo, float hi) {
+  if constexpr (PV16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    return pack_e4m3x2(lo, hi);
+  }
+}
+
+// P~ = fmt(2^(S*c + bias)) for keys [0, limit) (0 beyond), written to the row's swizzled
 // P buffer; returns the row sum of the unquantised values.
+template <bool PV16>
 __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, float bias,
                                               uint8_t* my_p, int r) {
   float a0 = 0.f, a1 = 0.f;
@@ -130,7 +157,7 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const float cgc = pick8(cg.v, 2 * ch + half);
-      uint32_t w4[4];
+      uint32_t w[PV16 ? 8 : 4];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         float e[4];
@@ -141,10 +168,14 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
         }
         add2(a0, a1, a0, a1, e[0], e[1]);
         add2(a0, a1, a0, a1, e[2], e[3]);
-        w4[q4] = pack_e4m3x2(e[0], e[1]) | (pack_e4m3x2(e[2], e[3]) << 16);
+        if constexpr (PV16) {
+          w[2 * q4] = pack_p2<true>(e[0], e[1]);
+          w[2 * q4 + 1] = pack_p2<true>(e[2], e[3]);
+        } else {
+          w[q4] = pack_p2<false>(e[0], e[1]) | (pack_p2<false>(e[2], e[3]) << 16);
+        }
       }
-      *reinterpret_cast<uint4*>(my_p + (((2 * ch + half) ^ (r & 7)) << 4)) =
-          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      store_p_group<PV16>(my_p, r, 2 * ch + half, w);
     }
   }
   return a0 + a1;
@@ -156,11 +187,11 @@ __device__ __forceinline__ void trace(const Problem& p, bool on, int role, int t
     p.dbg_trace[(role * kTraceTiles + tile) * kTraceEvents + ev] = clock64();
 }
 
-template <int DP>
+template <int DP, bool PV16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Problem p) {
-  using C = AttnCfg<DP>;
+  using C = AttnCfg<DP, PV16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -267,7 +298,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) break;
         trace(p, tr, 3, j, 1);
         mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
-        tma_load_3d(sV + sv * C::kVTileBytes, &tmV, &v_full[sv], krow, 0, (int)plane_kv);
+        if constexpr (PV16) {
+          // fp16 V^T: two 64-key chunks of DP rows x 128 bytes
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(sV + sv * C::kVTileBytes + c * DP * 128, &tmV, &v_full[sv], krow + c * 64, 0,
+                        (int)plane_kv);
+        } else {
+          tma_load_3d(sV + sv * C::kVTileBytes, &tmV, &v_full[sv], krow, 0, (int)plane_kv);
+        }
         ++issued_v;
       }
       if (!ok) {
@@ -310,9 +348,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t px =
             dp + static_cast<uint64_t>(((x * C::kPBufs + buf) * C::kPTileBytes) >> 4);
         const uint64_t vst = dv + static_cast<uint64_t>((sv * C::kVTileBytes) >> 4);
+        if constexpr (PV16) {
+          // K = 128 keys in steps of 16 (32 bytes) inside 64-key chunks
 #pragma unroll
-        for (int k = 0; k < kTileKeys / 32; ++k)
-          mma_f8_ss(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kTileKeys / 16; ++k) {
+            const uint32_t op = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
+            const uint32_t ov = ((k >> 2) * (DP * 128) + (k & 3) * 32) >> 4;
+            mma_f16_ss(d_o, px + op, vst + ov, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kTileKeys / 32; ++k)
+            mma_f8_ss(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+        }
         mma_commit(&o_full[x]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(&k_full[0], 0, abort_flag);
@@ -371,7 +419,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const bool active_tile = x == 0 || has_b;
     const int i = q_start + x * kTileRows + r;  // query row within the sequence
     const bool row_valid = active_tile && r < xrows;
-    const float log2_sigma = p.acc_mode == 1 ? 0.0f : 8.807354922057604f;  // log2(448)
+    // sigma_P: 448 for E4M3 P in the fp32 modes, 1 for fp16+fp32 and for fp16 P
+    const float log2_sigma = (PV16 || p.acc_mode == 1) ? 0.0f : 8.807354922057604f;  // log2(448)
     const bool trs = tr && (warp & 3) == 0 && lane == 0;
     float sq = 0.f;
     if (row_valid) sq = __ldg(&p.sq[plane_q * p.sq_pp + (s.row0_q + i) / p.gq]);
@@ -460,7 +509,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             float a0 = 0.f, a1 = 0.f;
-            uint32_t w4[4];
+            uint32_t w[PV16 ? 8 : 4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int c = g * 16 + q4 * 4;
@@ -472,16 +521,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
               add2(a0, a1, a0, a1, e0, e1);
               add2(a0, a1, a0, a1, e2, e3);
-              w4[q4] = pack_e4m3x2(e0, e1) | (pack_e4m3x2(e2, e3) << 16);
+              if constexpr (PV16) {
+                w[2 * q4] = pack_p2<true>(e0, e1);
+                w[2 * q4 + 1] = pack_p2<true>(e2, e3);
+              } else {
+                w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
+              }
             }
-            *reinterpret_cast<uint4*>(my_p + ((g ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            store_p_group<PV16>(my_p, r, g, w);
             add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
           }
         } else {
           Mult8 c8;
 #pragma unroll
           for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
-          gsum[0] = masked_tile_exp(tS, limit, c8, bias, my_p, r);
+          gsum[0] = masked_tile_exp<PV16>(tS, limit, c8, bias, my_p, r);
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
         // next tile's K scales (used one tile from now)
@@ -607,23 +661,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-size_t attention_smem_bytes(int dp) { return dp == 64 ? AttnCfg<64>::kSmem : AttnCfg<128>::kSmem; }
+template <int DP, bool PV16>
+static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
+  constexpr int smem = AttnCfg<DP, PV16>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_kernel<DP, PV16><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
                              cudaStream_t stream) {
   const dim3 grid(p.hq, grid_pairs, p.batch);
-  if (p.dp == 64) {
-    constexpr int smem = AttnCfg<64>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_kernel<64><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
-  } else {
-    constexpr int smem = AttnCfg<128>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_kernel<128><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
-  }
-  return cudaGetLastError();
+  if (p.pv16) return p.dp == 64 ? launch_attn_t<64, true>(p, maps, grid, stream)
+                                : launch_attn_t<128, true>(p, maps, grid, stream);
+  return p.dp == 64 ? launch_attn_t<64, false>(p, maps, grid, stream)
+                    : launch_attn_t<128, false>(p, maps, grid, stream);
 }
 
 }  // namespace sage

@@ -15,7 +15,6 @@ cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, in
 cudaError_t launch_export_vt(const uint8_t* vt, int64_t pitch, int dp, int d, int planes, int n,
                              uint8_t* out, cudaStream_t st);
 cudaError_t launch_e4m3(const float* x, uint8_t* out, int64_t n, cudaStream_t st);
-size_t attention_smem_bytes(int dp);
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
                              cudaStream_t stream);
 }  // namespace sage

@@ -26,6 +26,7 @@ struct Problem {
   int gq, gk, lgk;                 // token-group sizes of Q and K scales; lgk = log2(gk)
   int acc_mode;                    // 0: fp32 (P scaled by 448), 1: fp16 partials + fp32
   int vec16;                       // inputs allow 16-byte vector loads
+  int pv16;                        // FP16 P·V variant: V^T stored as fp16, P in fp16
   float sm_scale;
   float range_limit;               // smallest float >= 2^38 / N (dense only; varlen per seq)
   const void* q; int64_t q_sb, q_sh, q_sn;
@@ -40,11 +41,11 @@ struct Problem {
   int* err;
   long long* ksum; long long* vsum; int* vmin; int* vmax;   // [batch*hkv*d]
   float* kmean; float* vmean; float* vscale; float* vrcp;     // [batch*hkv*d]
-  __half* qc; __half* kc; uint8_t* vt;                        // codes
+  __half* qc; __half* kc; uint8_t* vt;  // codes; vt holds E4M3 bytes or (pv16) fp16 V^T
   float* sq; float* sk; float* qkc;                           // scales, LSE correction
   int* seqinfo;                    // varlen: [kSiRows][batch] per-sequence geometry + LPT order
   int64_t q_rows, k_rows;          // rows per plane in qc / kc (dense: nq / nk)
-  int64_t vt_pitch;                // bytes per channel row of vt
+  int64_t vt_pitch;                // elements per channel row of vt (1 or 2 bytes each)
   int64_t sq_pp, sk_pp;            // scale groups per plane
   int32_t* dbg_scores;             // optional exact-score dump [B,Hq,Nq,Nk]
   int dbg_stall;                   // test hook: the producer issues no K/V loads

@@ -236,8 +236,9 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
   const float amax = fmaxf(fabsf(mx), fabsf(mn));
   p.kmean[i] = km;
   p.vmean[i] = vm;
-  p.vscale[i] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
-  p.vrcp[i] = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+  // the FP16 P·V variant keeps V' unscaled
+  p.vscale[i] = p.pv16 ? 1.0f : (amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f);
+  p.vrcp[i] = p.pv16 ? 1.0f : (amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -249,6 +250,7 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //   K: K' = K - kmean, INT8 per group of gk rows.
 //   V: V' = V - vmean, E4M3 with the per-channel scale absmax/448, written transposed
 //      [channel][token] so that P.V reads V^T tiles K-major.
+//   V (kind 3, FP16 P·V variant): V' = V - vmean rounded to fp16 (RNE), transposed likewise.
 // Rows past the sequence end up to the stored tile end are written as zeros.
 template <typename T, int kind, int TPR>
 __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
@@ -270,7 +272,6 @@ __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p)
 
   __shared__ float rowmax[kTileRows];
   __shared__ float grcp[kTileRows];
-  __shared__ __align__(16) uint8_t vtile[128][kTileRows];
 
   // per-channel values from the finalize pass: smoothing means, V scale reciprocals, and for
   // Q heads the K mean used by the LSE term
@@ -279,7 +280,8 @@ __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const bool ch = c0 + i < d;
-    mean[i] = (ch && kind == 1) ? p.kmean[sidx + c0 + i] : ((ch && kind == 2) ? p.vmean[sidx + c0 + i] : 0.f);
+    mean[i] = (ch && kind == 1) ? p.kmean[sidx + c0 + i]
+                                : ((ch && kind >= 2) ? p.vmean[sidx + c0 + i] : 0.f);
     rcpv[i] = (ch && kind == 2) ? p.vrcp[sidx + c0 + i] : 0.f;
     kmean_q[i] = (ch && want_qkc) ? p.kmean[sidx + c0 + i] : 0.f;
   }
@@ -311,8 +313,36 @@ __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p)
     for (int j = 0; j < 8; ++j) x[j] = (live && c0 + j < d) ? __fsub_rn(x[j], mean[j]) : 0.f;
   };
 
-  if (kind == 2) {
+  if constexpr (kind == 3) {
+    // ---- V: fp16 values, transposed through shared memory. Element (channel c, token rr)
+    // sits at column rr ^ (8 * ((c >> 3) & 15)): whole 16-byte units move, and the 16 threads
+    // of a row (one channel octet each) hit different banks.
+    __shared__ __align__(16) __half vtile16[128][kTileRows];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int rr = rg + RG * i;
+      float x[8];
+      row_values(i, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) vtile16[c0 + j][rr ^ ((vec & 15) << 3)] = __float2half_rn(x[j]);
+    }
+    __syncthreads();
+    const int64_t plane = plane_of(p, b, h, p.hkv);
+    const int64_t col0 = (int64_t)s.row0_k + r0;
+    const int ncols = (int)min((int64_t)kTileRows, p.vt_pitch - col0);
+    __half* vt16 = reinterpret_cast<__half*>(p.vt);
+    for (int idx = threadIdx.x; idx < dp * 16; idx += 256) {
+      const int c = idx >> 4, u = idx & 15;  // channel, 8-token unit
+      if (u * 8 < ncols) {
+        const uint4 val = *reinterpret_cast<const uint4*>(&vtile16[c][(u ^ ((c >> 3) & 15)) << 3]);
+        *reinterpret_cast<uint4*>(vt16 + (plane * dp + c) * p.vt_pitch + col0 + u * 8) = val;
+      }
+    }
+    return;
+  }
+  if constexpr (kind == 2) {
     // ---- V: E4M3 codes, transposed through shared memory
+    __shared__ __align__(16) uint8_t vtile[128][kTileRows];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int rr = rg + RG * i;
@@ -496,11 +526,13 @@ static void launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaS
   if (p.dp == 64) {
     quant_kernel<T, 0, 8><<<gq, 256, 0, st>>>(p);
     quant_kernel<T, 1, 8><<<gk, 256, 0, st>>>(p);
-    quant_kernel<T, 2, 8><<<gk, 256, 0, st>>>(p);
+    if (p.pv16) quant_kernel<T, 3, 8><<<gk, 256, 0, st>>>(p);
+    else quant_kernel<T, 2, 8><<<gk, 256, 0, st>>>(p);
   } else {
     quant_kernel<T, 0, 16><<<gq, 256, 0, st>>>(p);
     quant_kernel<T, 1, 16><<<gk, 256, 0, st>>>(p);
-    quant_kernel<T, 2, 16><<<gk, 256, 0, st>>>(p);
+    if (p.pv16) quant_kernel<T, 3, 16><<<gk, 256, 0, st>>>(p);
+    else quant_kernel<T, 2, 16><<<gk, 256, 0, st>>>(p);
   }
 }
 

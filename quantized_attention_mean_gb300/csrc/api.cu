@@ -82,8 +82,8 @@ void carve(Problem& p, const Layout& L, void* ws) {
   p.err = reinterpret_cast<int*>(w + L.off_err);
   p.ksum = reinterpret_cast<long long*>(w + L.off_ksum);
   p.vsum = reinterpret_cast<long long*>(w + L.off_vsum);
-  p.vmin = reinterpret_cast<int*>(w + L.off_vmin);
-  p.vmax = reinterpret_cast<int*>(w + L.off_vmax);
+  p.vmin = reinterpret_cast<unsigned*>(w + L.off_vmin);
+  p.vmax = reinterpret_cast<unsigned*>(w + L.off_vmax);
   p.kmean = reinterpret_cast<float*>(w + L.off_kmean);
   p.vmean = reinterpret_cast<float*>(w + L.off_vmean);
   p.vscale = reinterpret_cast<float*>(w + L.off_vscale);
@@ -247,9 +247,10 @@ int run_pipeline(Problem& p, const Layout& L, int max_len_q, int max_len_k, cuda
   auto mark = [&](int i) { if (ev) cudaEventRecord(ev->e[i], st); };
   cudaError_t e;
   mark(0);
-  if ((e = cudaMemsetAsync(p.err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "status reset");
+  // status and statistics accumulators (contiguous from off_err up to off_kmean): one clear
+  if ((e = cudaMemsetAsync(p.err, 0, L.off_kmean - L.off_err, st)) != cudaSuccess)
+    return cuda_fail(e, "status and statistics reset");
   if (p.varlen && (e = launch_varlen_setup(p, st)) != cudaSuccess) return cuda_fail(e, "varlen set-up");
-  if ((e = launch_reset(p, static_cast<int>(L.n_stats), st)) != cudaSuccess) return cuda_fail(e, "statistics reset");
   if ((e = launch_kv_stats(p, max_len_k, st)) != cudaSuccess) return cuda_fail(e, "K/V statistics");
   if ((e = launch_finalize(p, static_cast<int>(L.n_stats), st)) != cudaSuccess) return cuda_fail(e, "statistics finalize");
   mark(1);

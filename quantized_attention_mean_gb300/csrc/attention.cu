@@ -46,8 +46,8 @@ struct AttnCfg {
   static constexpr int kKStages = DP == 128 ? 2 : 3;
   static constexpr int kVStages = DP == 128 ? (PV16 ? 1 : 2) : 3;
   // P buffers per query tile: with two, the softmax writes P_j while P.V of tile j - 1 may
-  // still be reading P_{j-1} (shared memory allows it for DP = 64 only)
-  static constexpr int kPBufs = DP == 64 && !PV16 ? 2 : 1;
+  // still be reading P_{j-1} (the FP16 P·V variant has room for one)
+  static constexpr int kPBufs = PV16 ? 1 : 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;

@@ -6,7 +6,6 @@
 
 namespace sage {
 cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st);
-cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st);
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st);
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st);
 cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st);

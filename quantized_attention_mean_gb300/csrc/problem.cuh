@@ -39,7 +39,8 @@ struct Problem {
   int total_q, total_k;
   // workspace
   int* err;
-  long long* ksum; long long* vsum; int* vmin; int* vmax;   // [batch*hkv*d]
+  long long* ksum; long long* vsum;                           // [batch*hkv*d]
+  unsigned* vmin; unsigned* vmax;  // [batch*hkv*d] order-preserving codes, zero = empty
   float* kmean; float* vmean; float* vscale; float* vrcp;     // [batch*hkv*d]
   __half* qc; __half* kc; uint8_t* vt;  // codes; vt holds E4M3 bytes or (pv16) fp16 V^T
   float* sq; float* sk; float* qkc;                           // scales, LSE correction
@@ -125,13 +126,15 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Order-preserving float <-> int map for atomicMin / atomicMax on floats.
-__device__ __forceinline__ int float_to_ordered(float f) {
-  int i = __float_as_int(f);
-  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+// Order-preserving float -> unsigned map (a larger float has a larger code, and every
+// non-NaN float's code is above 0), so a zero-filled buffer is an empty atomicMax
+// accumulator. The minimum is kept as the maximum of the complemented code.
+__device__ __forceinline__ unsigned ordered_code(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ float ordered_to_float(int i) {
-  return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF);
+__device__ __forceinline__ float ordered_decode(unsigned c) {
+  return __uint_as_float((c & 0x80000000u) ? (c & 0x7FFFFFFFu) : ~c);
 }
 
 // Adding 1.5 * 2^23 rounds an fp32 value v with |v| < 2^22 to an integer (ties to even, the

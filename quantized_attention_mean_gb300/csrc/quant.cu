@@ -67,27 +67,15 @@ __global__ void __launch_bounds__(1024) varlen_setup_kernel(Problem p) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Workspace reset before the statistics pass: sums to 0, min / max to +inf / -inf.
-__global__ void ws_reset_kernel(Problem p, int n_stats) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_stats; i += gridDim.x * blockDim.x) {
-    p.ksum[i] = 0;
-    p.vsum[i] = 0;
-    p.vmin[i] = float_to_ordered(__int_as_float(0x7f800000));
-    p.vmax[i] = float_to_ordered(__int_as_float(0xff800000));
-  }
-}
-
-// ------------------------------------------------------------------------------------------
-// K/V statistics, one tensor per launch (KIND 0: K, the fixed-point sum, launched only with
+// K/V statistics of one block of tokens (KIND 0: K, the fixed-point sum, run only with
 // smooth_k; KIND 1: V, the fixed-point sum with smooth_v, and the min / max). Per (sequence,
 // kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads: thread = (row group rg,
 // channel vector vec); TPR = padded head_dim / 8 threads per row.
 template <typename T, int TPR, int KIND>
-__global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
+__device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int hk, int b) {
   constexpr int RG = 256 / TPR;
   constexpr int kRows = 4;                 // rows per thread
   constexpr int kChunk = kRows * RG;       // tokens per block: stats_chunk(8 * TPR)
-  const int chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int t0 = chunk * kChunk;
   if (t0 >= s.len_k) return;
@@ -201,7 +189,7 @@ __global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
     if (threadIdx.x < p.d) {
       float m = red_f[0][threadIdx.x];
       for (int w = 1; w < 8; ++w) m = fminf(m, red_f[w][threadIdx.x]);
-      atomicMin(&p.vmin[sidx + threadIdx.x], float_to_ordered(m));
+      atomicMax(&p.vmin[sidx + threadIdx.x], ~ordered_code(m));
     }
     __syncthreads();
     if (lane < TPR) {
@@ -212,9 +200,19 @@ __global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
     if (threadIdx.x < p.d) {
       float m = red_f[0][threadIdx.x];
       for (int w = 1; w < 8; ++w) m = fmaxf(m, red_f[w][threadIdx.x]);
-      atomicMax(&p.vmax[sidx + threadIdx.x], float_to_ordered(m));
+      atomicMax(&p.vmax[sidx + threadIdx.x], ordered_code(m));
     }
   }
+}
+
+// Both tensors' statistics in one launch. Grid: (token chunks, Hkv, batch x tensors): blockIdx.z
+// = b + batch * t, t = 0 for K (present only with smooth_k) and the last t for V.
+template <typename T, int TPR>
+__global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
+  const int b = blockIdx.z % p.batch;
+  const bool is_k = p.smooth_k && (int)blockIdx.z < p.batch;
+  if (is_k) kv_stats_block<T, TPR, 0>(p, blockIdx.x, blockIdx.y, b);
+  else kv_stats_block<T, TPR, 1>(p, blockIdx.x, blockIdx.y, b);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -231,8 +229,8 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
   if (s.len_k <= 0) return;
   const float km = p.smooth_k ? fixed_point_mean(p.ksum[i], s.len_k) : 0.f;
   const float vm = p.smooth_v ? fixed_point_mean(p.vsum[i], s.len_k) : 0.f;
-  const float mx = __fsub_rn(ordered_to_float(p.vmax[i]), vm);
-  const float mn = __fsub_rn(ordered_to_float(p.vmin[i]), vm);
+  const float mx = __fsub_rn(ordered_decode(p.vmax[i]), vm);
+  const float mn = __fsub_rn(ordered_decode(~p.vmin[i]), vm);
   const float amax = fmaxf(fabsf(mx), fabsf(mn));
   p.kmean[i] = km;
   p.vmean[i] = vm;
@@ -253,10 +251,9 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //   V (kind 3, FP16 P·V variant): V' = V - vmean rounded to fp16 (RNE), transposed likewise.
 // Rows past the sequence end up to the stored tile end are written as zeros.
 template <typename T, int kind, int TPR>
-__global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
+__device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, int b) {
   constexpr int RG = 256 / TPR;      // row groups
   constexpr int RPT = kTileRows / RG;  // rows per thread
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const Seq s = get_seq(p, b);
   const int len = kind == 0 ? s.len_q : s.len_k;
   // rows stored for this sequence: dense planes hold exactly len rows; varlen segments are
@@ -454,6 +451,16 @@ __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p)
   }
 }
 
+// Q, K and V quantisation in one launch. Grid: (128-token tiles of the longest sequence,
+// Hq + 2 Hkv, batch): blockIdx.y selects a Q head, then a K head, then a V head.
+template <typename T, int TPR, bool PV16>
+__global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
+  const int y = blockIdx.y;
+  if (y < p.hq) quant_block<T, 0, TPR>(p, blockIdx.x, y, blockIdx.z);
+  else if (y < p.hq + p.hkv) quant_block<T, 1, TPR>(p, blockIdx.x, y - p.hq, blockIdx.z);
+  else quant_block<T, PV16 ? 3 : 2, TPR>(p, blockIdx.x, y - p.hq - p.hkv, blockIdx.z);
+}
+
 // ------------------------------------------------------------------------------------------
 // Export of the quantised state in canonical layouts (test hook).
 __global__ void export_codes_kernel(const __half* codes, int64_t rows_pp, int dp, int d,
@@ -489,21 +496,11 @@ cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset(const Problem& p, int n_stats, cudaStream_t st) {
-  const int blocks = max(1, min(1024, (n_stats + 255) / 256));
-  ws_reset_kernel<<<blocks, 256, 0, st>>>(p, n_stats);
-  return cudaGetLastError();
-}
-
 template <typename T>
 static void launch_kv_stats_t(const Problem& p, dim3 grid, cudaStream_t st) {
-  if (p.dp == 64) {
-    if (p.smooth_k) kv_stats_kernel<T, 8, 0><<<grid, 256, 0, st>>>(p);
-    kv_stats_kernel<T, 8, 1><<<grid, 256, 0, st>>>(p);
-  } else {
-    if (p.smooth_k) kv_stats_kernel<T, 16, 0><<<grid, 256, 0, st>>>(p);
-    kv_stats_kernel<T, 16, 1><<<grid, 256, 0, st>>>(p);
-  }
+  grid.z *= p.smooth_k ? 2 : 1;
+  if (p.dp == 64) kv_stats_kernel<T, 8><<<grid, 256, 0, st>>>(p);
+  else kv_stats_kernel<T, 16><<<grid, 256, 0, st>>>(p);
 }
 
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
@@ -521,18 +518,14 @@ cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st) {
 
 template <typename T>
 static void launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
-  const dim3 gq((max_len_q + kTileRows - 1) / kTileRows, p.hq, p.batch);
-  const dim3 gk((max_len_k + kTileRows - 1) / kTileRows, p.hkv, p.batch);
+  const int len = max_len_q > max_len_k ? max_len_q : max_len_k;
+  const dim3 grid((len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
   if (p.dp == 64) {
-    quant_kernel<T, 0, 8><<<gq, 256, 0, st>>>(p);
-    quant_kernel<T, 1, 8><<<gk, 256, 0, st>>>(p);
-    if (p.pv16) quant_kernel<T, 3, 8><<<gk, 256, 0, st>>>(p);
-    else quant_kernel<T, 2, 8><<<gk, 256, 0, st>>>(p);
+    if (p.pv16) quant_kernel<T, 8, true><<<grid, 256, 0, st>>>(p);
+    else quant_kernel<T, 8, false><<<grid, 256, 0, st>>>(p);
   } else {
-    quant_kernel<T, 0, 16><<<gq, 256, 0, st>>>(p);
-    quant_kernel<T, 1, 16><<<gk, 256, 0, st>>>(p);
-    if (p.pv16) quant_kernel<T, 3, 16><<<gk, 256, 0, st>>>(p);
-    else quant_kernel<T, 2, 16><<<gk, 256, 0, st>>>(p);
+    if (p.pv16) quant_kernel<T, 16, true><<<grid, 256, 0, st>>>(p);
+    else quant_kernel<T, 16, false><<<grid, 256, 0, st>>>(p);
   }
 }
 

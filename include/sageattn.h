@@ -169,6 +169,18 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
                      int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* The FP16 P·V variant of sage_attn_varlen (see sage_attn_qk_int8_pv_fp16): same arguments,
+ * workspace size and errors; V' and P in fp16 on the tensor cores. */
+int sage_attn_varlen_qk_int8_pv_fp16(const sage_packed* q, const sage_packed* k,
+                                     const sage_packed* v, const sage_packed* out, float* lse,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int batch, int max_seqlen_q, int max_seqlen_k, int total_q,
+                                     int total_k, int heads_q, int heads_kv, int head_dim,
+                                     int dtype, int is_causal, float sm_scale, int return_lse,
+                                     int qk_quant_gran, int pv_accum_dtype, int smooth_k,
+                                     int smooth_v, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* Composition of partial results over disjoint key sets (pwwt.cn "SageAttention deployment
  * pitfalls guide" §4.1: return_lse exists for Ring Attention and similar schemes, which attend
  * to chunks of the keys separately). For every (b, h, n) row:

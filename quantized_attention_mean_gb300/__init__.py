@@ -135,9 +135,10 @@ def sage_attn_qk_int8_pv_fp16(q, k, v, tensor_layout="HND", is_causal=False, sm_
 def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                      is_causal=False, sm_scale=None, return_lse=False, qk_quant_gran="per_warp",
                      pv_accum_dtype="fp32", smooth_k=True, smooth_v=False, out=None, lse=None,
-                     workspace=None, stream=None):
+                     workspace=None, stream=None, pv="fp8"):
     """Variable-length forward: q [Tq, Hq, d], k/v [Tk, Hkv, d], cu_seqlens int32 [B+1] on the
-    device. Returns out [Tq, Hq, d] (+ lse [Hq, Tq] fp32 if return_lse)."""
+    device. Returns out [Tq, Hq, d] (+ lse [Hq, Tq] fp32 if return_lse). pv="fp16" selects the
+    FP16 P·V variant."""
     lib = _lib.load()
     if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
@@ -155,7 +156,10 @@ def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         workspace = alloc_workspace(need, q.device)
     scale = float("nan") if sm_scale is None else float(sm_scale)
     with torch.cuda.device(q.device):
-        st = lib.sage_attn_varlen(
+        if pv not in ("fp8", "fp16"):
+            raise ValueError("pv must be 'fp8' or 'fp16'")
+        entry = lib.sage_attn_varlen_qk_int8_pv_fp16 if pv == "fp16" else lib.sage_attn_varlen
+        st = entry(
             ctypes.byref(_packed(q)), ctypes.byref(_packed(k)), ctypes.byref(_packed(v)),
             ctypes.byref(_packed(out)), ctypes.c_void_p(lse.data_ptr() if return_lse else 0),
             ctypes.c_void_p(cu_seqlens_q.data_ptr()), ctypes.c_void_p(cu_seqlens_k.data_ptr()),

@@ -35,6 +35,9 @@ SIGNATURES = {
     "sage_attn_varlen_workspace_size": (c_size_t, [c_int] * 7),
     "sage_attn_varlen": (c_int, [_P, _P, _P, _P, c_void_p, c_void_p, c_void_p] + [c_int] * 10
                          + [c_float] + [c_int] * 5 + [c_void_p, c_size_t, c_void_p]),
+    "sage_attn_varlen_qk_int8_pv_fp16": (c_int, [_P, _P, _P, _P, c_void_p, c_void_p, c_void_p]
+                                         + [c_int] * 10 + [c_float] + [c_int] * 5
+                                         + [c_void_p, c_size_t, c_void_p]),
     "sage_status_string": (ctypes.c_char_p, [c_int]),
     "sage_last_cuda_error": (ctypes.c_char_p, []),
     "sage_read_device_status": (c_int, [c_void_p, c_void_p]),

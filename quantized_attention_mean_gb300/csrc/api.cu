@@ -373,13 +373,13 @@ size_t sage_attn_varlen_workspace_size(int batch, int heads_q, int heads_kv, int
   return L.total;
 }
 
-int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_packed* v,
-                     const sage_packed* out, float* lse, const int32_t* cu_seqlens_q,
-                     const int32_t* cu_seqlens_k, int batch, int max_seqlen_q, int max_seqlen_k,
-                     int total_q, int total_k, int heads_q, int heads_kv, int head_dim, int dtype,
-                     int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
-                     int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+static int varlen_impl(const sage_packed* q, const sage_packed* k, const sage_packed* v,
+                       const sage_packed* out, float* lse, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int batch, int max_seqlen_q, int max_seqlen_k,
+                       int total_q, int total_k, int heads_q, int heads_kv, int head_dim, int dtype,
+                       int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+                       int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
+                       size_t workspace_bytes, void* stream, int pv16) {
   if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return SAGE_ERR_INVALID_ARG;
   const Common c{heads_q, heads_kv, head_dim, dtype, is_causal, return_lse, qk_quant_gran,
                  pv_accum_dtype, smooth_k, smooth_v, sm_scale};
@@ -408,6 +408,7 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
   fill_common(p, c);
   p.batch = batch; p.nq = max_seqlen_q; p.nk = max_seqlen_k; p.varlen = 1;
   p.vec16 = vec16 ? 1 : 0;
+  p.pv16 = pv16;
   p.total_q = total_q; p.total_k = total_k;
   p.cu_q = cu_seqlens_q; p.cu_k = cu_seqlens_k;
   p.q = q->data; p.q_sb = 0; p.q_sn = q->stride_token; p.q_sh = q->stride_head;
@@ -420,6 +421,34 @@ int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_pack
   p.dbg_stall = g_stall;
   carve(p, L, workspace);
   return run_pipeline(p, L, max_seqlen_q, max_seqlen_k, static_cast<cudaStream_t>(stream));
+}
+
+int sage_attn_varlen(const sage_packed* q, const sage_packed* k, const sage_packed* v,
+                     const sage_packed* out, float* lse, const int32_t* cu_seqlens_q,
+                     const int32_t* cu_seqlens_k, int batch, int max_seqlen_q, int max_seqlen_k,
+                     int total_q, int total_k, int heads_q, int heads_kv, int head_dim, int dtype,
+                     int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+                     int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return varlen_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q,
+                     max_seqlen_k, total_q, total_k, heads_q, heads_kv, head_dim, dtype, is_causal,
+                     sm_scale, return_lse, qk_quant_gran, pv_accum_dtype, smooth_k, smooth_v,
+                     workspace, workspace_bytes, stream, 0);
+}
+
+int sage_attn_varlen_qk_int8_pv_fp16(const sage_packed* q, const sage_packed* k,
+                                     const sage_packed* v, const sage_packed* out, float* lse,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int batch, int max_seqlen_q, int max_seqlen_k, int total_q,
+                                     int total_k, int heads_q, int heads_kv, int head_dim,
+                                     int dtype, int is_causal, float sm_scale, int return_lse,
+                                     int qk_quant_gran, int pv_accum_dtype, int smooth_k,
+                                     int smooth_v, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return varlen_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q,
+                     max_seqlen_k, total_q, total_k, heads_q, heads_kv, head_dim, dtype, is_causal,
+                     sm_scale, return_lse, qk_quant_gran, pv_accum_dtype, smooth_k, smooth_v,
+                     workspace, workspace_bytes, stream, 1);
 }
 
 const char* sage_status_string(int status) {

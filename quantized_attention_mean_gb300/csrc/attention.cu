@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the quantised operands and scales come from the previous kernel in the stream
+  pdl_wait();
 
   if (warp >= 8) {
    regs_dec<kRegsControl>();
@@ -666,8 +668,8 @@ static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3
   constexpr int smem = AttnCfg<DP, PV16>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_kernel<DP, PV16><<<grid, kAttnThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<DP, PV16>, grid, dim3(kAttnThreads), smem, stream, maps[0], maps[1],
+                    maps[2], p);
 }
 
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,

@@ -5,6 +5,24 @@
 #include "problem.cuh"
 
 namespace sage {
+// Programmatic dependent launch: the kernel may start while the previous kernel in the
+// stream is finishing; it must execute pdl_wait() before it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st);
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st);
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st);

@@ -83,6 +83,12 @@ __device__ __forceinline__ int64_t plane_of(const Problem& p, int b, int h, int 
 
 __device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
 
+// Programmatic dependent launch (no-ops for kernels launched without it): wait until the
+// previous kernel in the stream has completed and its writes are visible; let the next
+// kernel begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {

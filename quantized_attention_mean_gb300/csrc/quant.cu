@@ -209,6 +209,7 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
 // = b + batch * t, t = 0 for K (present only with smooth_k) and the last t for V.
 template <typename T, int TPR>
 __global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
+  pdl_trigger();
   const int b = blockIdx.z % p.batch;
   const bool is_k = p.smooth_k && (int)blockIdx.z < p.batch;
   if (is_k) kv_stats_block<T, TPR, 0>(p, blockIdx.x, blockIdx.y, b);
@@ -222,6 +223,8 @@ __global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
 // this equals the max over tokens of |fl32(v - vmean)|). Computed once here so the
 // quantisation pass needs no double-precision arithmetic.
 __global__ void kv_finalize_kernel(Problem p, int n_stats) {
+  pdl_trigger();
+  pdl_wait();  // the statistics kernel's sums
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_stats) return;
   const int b = i / (p.hkv * p.d);
@@ -455,6 +458,8 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 // Hq + 2 Hkv, batch): blockIdx.y selects a Q head, then a K head, then a V head.
 template <typename T, int TPR, bool PV16>
 __global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
+  pdl_trigger();
+  pdl_wait();  // the finalisation's means and scales
   const int y = blockIdx.y;
   if (y < p.hq) quant_block<T, 0, TPR>(p, blockIdx.x, y, blockIdx.z);
   else if (y < p.hq + p.hkv) quant_block<T, 1, TPR>(p, blockIdx.x, y - p.hq, blockIdx.z);
@@ -512,27 +517,28 @@ cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
 }
 
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st) {
-  kv_finalize_kernel<<<(n_stats + 255) / 256, 256, 0, st>>>(p, n_stats);
+  const cudaError_t e = launch_pdl(kv_finalize_kernel, dim3((n_stats + 255) / 256), dim3(256), 0, st, p, n_stats);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <typename T>
-static void launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
+static cudaError_t launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
   const int len = max_len_q > max_len_k ? max_len_q : max_len_k;
   const dim3 grid((len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
   if (p.dp == 64) {
-    if (p.pv16) quant_kernel<T, 8, true><<<grid, 256, 0, st>>>(p);
-    else quant_kernel<T, 8, false><<<grid, 256, 0, st>>>(p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true>, grid, dim3(256), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 8, false>, grid, dim3(256), 0, st, p);
   } else {
-    if (p.pv16) quant_kernel<T, 16, true><<<grid, 256, 0, st>>>(p);
-    else quant_kernel<T, 16, false><<<grid, 256, 0, st>>>(p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true>, grid, dim3(256), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 16, false>, grid, dim3(256), 0, st, p);
   }
 }
 
 cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
-  if (p.dtype == 0) launch_quant_t<__half>(p, max_len_q, max_len_k, st);
-  else launch_quant_t<__nv_bfloat16>(p, max_len_q, max_len_k, st);
-  return cudaGetLastError();
+  const cudaError_t e = p.dtype == 0 ? launch_quant_t<__half>(p, max_len_q, max_len_k, st)
+                                     : launch_quant_t<__nv_bfloat16>(p, max_len_q, max_len_k, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, int d, int planes,

@@ -22,7 +22,7 @@ CASES = [
 ]
 
 
-def _run(w, lens):
+def _run(w, lens, pv="fp8"):
     import quantized_attention_mean_gb300 as qa
     q, k, v, cu_q, cu_k, lens = varlen_inputs(w, 0, lens)
     dev = torch.device("cuda:0")
@@ -32,20 +32,22 @@ def _run(w, lens):
                                                       w.d, w.gran), dev)
     res = qa.sage_attn_varlen(qd, kd, vd, cqd, ckd, max(lens), max(lens), is_causal=w.is_causal,
                               return_lse=w.return_lse, qk_quant_gran=w.gran, pv_accum_dtype=w.accum,
-                              smooth_k=w.smooth_k, smooth_v=w.smooth_v, workspace=ws)
+                              smooth_k=w.smooth_k, smooth_v=w.smooth_v, workspace=ws, pv=pv)
     out, lse = res if w.return_lse else (res, None)
     torch.cuda.synchronize()
     assert qa.read_device_status(ws) == 0
     qn, kn, vn = (t.float().numpy() for t in (q, k, v))
     ref = sage_attention_varlen(qn, kn, vn, cu_q.numpy(), cu_k.numpy(), is_causal=w.is_causal,
                                 gran=GRAN[w.gran], accum=ACC[w.accum], smooth_k=w.smooth_k,
-                                smooth_v=w.smooth_v)
+                                smooth_v=w.smooth_v, pv=pv)
     return qn, kn, vn, cu_q.numpy(), out.float().cpu().numpy(), (lse.cpu().numpy() if lse is not None else None), ref
 
 
+@pytest.mark.parametrize("pv", ["fp8", "fp16"])
 @pytest.mark.parametrize("w,lens", CASES, ids=[c[0].name for c in CASES])
-def test_varlen_parity(w, lens):
-    qn, kn, vn, cu, o, lse, ref = _run(w, lens)
+def test_varlen_parity(w, lens, pv):
+    # pv="fp16": the FP16 P·V variant against the oracle's pv="fp16" emulation
+    qn, kn, vn, cu, o, lse, ref = _run(w, lens, pv)
     assert np.isfinite(o).all()
     assert max_abs_excess(o, ref["o"], w.dtype) <= TOL_MAX_ABS
     assert cosine(o, ref["o"]) >= TOL_COS

@@ -255,7 +255,8 @@ int sage_debug_stall_attention(int on);
 /* Pipeline trace hook: while `clocks` (device, 4*64*8 int64, caller-owned) is non-NULL, dense
  * calls record clock64() of the first CTA's pipeline events there: [role][tile][event] with
  * role 0/1 = softmax of query tile A/B (events: scores ready, scores loaded, max done,
- * exponentials done, P buffer free, P written, O rescaled), role 2 = MMA issue (per tile x:
+ * exponentials done, P buffer free, P written, O rescaled; event 7 of the last tile: output
+ * written), role 2 = MMA issue (per tile x:
  * 4x+0 P ready, 4x+1 QK^T issued, 4x+2 O ready, 4x+3 P.V issued), role 3 = TMA (K, V
  * issued), for the first 64 KV tiles. NULL turns it off. Process-wide. Returns SAGE_OK. */
 int sage_debug_trace_attention(long long* clocks);

@@ -73,6 +73,43 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// a[idx] for a runtime idx in [0, 32) without indexing a register array.
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&a)[32], int idx) {
+  uint32_t v = a[0];
+#pragma unroll
+  for (int g = 1; g < 32; ++g) v = idx == g ? a[g] : v;
+  return v;
+}
+
+// Two output values as fp16 (dtype 0) or bf16 bits, the first in the low half.
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int dtype) {
+  if (dtype == 0) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// V scales and means of the channels [c0, c0 + 32) as 16-byte loads, 8-channel groups at or
+// past d left zero (d % 8 == 0; the rows start 32-byte aligned).
+__device__ __forceinline__ void load_chunk_scales(const float* vsc, const float* vmn, int c0, int d,
+                                                  float4 (&cs)[8], float4 (&cm)[8]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (c0 + q * 8 < d) {
+      const float4* s4 = reinterpret_cast<const float4*>(vsc + c0 + q * 8);
+      const float4* m4 = reinterpret_cast<const float4*>(vmn + c0 + q * 8);
+      cs[2 * q] = __ldg(s4);
+      cs[2 * q + 1] = __ldg(s4 + 1);
+      cm[2 * q] = __ldg(m4);
+      cm[2 * q + 1] = __ldg(m4 + 1);
+    } else {
+      cs[2 * q] = cs[2 * q + 1] = cm[2 * q] = cm[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
 // a[idx] for a runtime idx in [0, 8) without indexing a register array.
 __device__ __forceinline__ float pick8(const float (&a)[8], int idx) {
   float v = a[0];
@@ -587,66 +624,102 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&o_ready[x]);
         trace(p, trs, x, j, 6);
       }
-      // ---- epilogue
+      // ---- epilogue: out = acc . s_v / l + v_mean, then the LSE. The output address, the LSE
+      // term and the first chunk's V scales / means are fetched while P.V of the last tile
+      // completes, and each 32-channel chunk's scales are requested before the previous
+      // chunk's values are stored. The chunk loop stays rolled: it runs once per CTA, from a
+      // cold instruction cache. Rows of 16-byte chunks (head_dim % 8 == 0) are stored 16
+      // bytes at a time; with head_dim 64 each thread first puts its row into this tile's P
+      // buffers (free once the last P.V is done), XOR-swizzled by chunk so that neither side
+      // conflicts on banks, and each warp then writes its 32 rows out whole, four rows per
+      // store instruction (measured: faster than direct row stores for head_dim 64, slower
+      // for 128).
+      const float* vsc = p.vscale + ((int64_t)b * p.hkv + hk) * p.d;
+      const float* vmn = p.vmean + ((int64_t)b * p.hkv + hk) * p.d;
+      uint16_t* const dst = static_cast<uint16_t*>(p.o) + (int64_t)b * p.o_sb +
+                            (int64_t)(s.tok0_q + i) * p.o_sn + (int64_t)h * p.o_sh;
+      constexpr bool kStageOut = DP == 64;
+      constexpr int kSwz = DP / 8 - 1;  // 16-byte chunks of a staged row, minus one
+      uint8_t* const stage = sP + x * C::kPBufs * C::kPTileBytes;  // [128 rows][DP * 2 bytes]
+      static_assert(kTileRows * DP * 2 <= C::kPBufs * C::kPTileBytes, "output staging fits in P");
+      const bool vec = p.vec16 != 0;  // head_dim % 8 == 0, 16-byte aligned output rows
+      float qk_term = 0.f;
+      if (p.return_lse && p.smooth_k && row_valid) qk_term = p.qkc[plane_q * p.q_rows + s.row0_q + i];
+      float4 cs[8], cm[8];  // V scales / means of the current chunk's 32 channels
+      if (vec) load_chunk_scales(vsc, vmn, 0, p.d, cs, cm);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (n_tiles - 1) & 1, abort_flag));
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.0f / l;
-        const float* vsc = p.vscale + ((int64_t)b * p.hkv + hk) * p.d;
-        const float* vmn = p.vmean + ((int64_t)b * p.hkv + hk) * p.d;
-        const int64_t orow = (int64_t)b * p.o_sb + (int64_t)(s.tok0_q + i) * p.o_sn + (int64_t)h * p.o_sh;
-#pragma unroll
-        for (int cc = 0; cc < DP / 32; ++cc) {
+#pragma unroll 1
+        for (int cc = 0; cc < DP / 32 && cc * 32 < p.d; ++cc) {
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
+          float4 ns[8], nm[8];
+          const bool more = vec && cc + 1 < DP / 32 && (cc + 1) * 32 < p.d;
+          if (more) load_chunk_scales(vsc, vmn, (cc + 1) * 32, p.d, ns, nm);
           tmem_wait_ld(o);
-          if (row_valid && cc * 32 < p.d) {
-            float v[32];
+          if (row_valid) {
+            if (vec) {
+              // whole 8-channel groups (head_dim % 8 == 0), one 16-byte store each
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const int c = cc * 32 + u;
-              v[u] = c < p.d ? fmaf(__uint_as_float(o[u]) * __ldg(&vsc[c]), inv_l, __ldg(&vmn[c])) : 0.f;
-            }
-            if (p.dtype == 0) {
-              __half* dst = static_cast<__half*>(p.o) + orow + cc * 32;
-              if (p.vec16 && cc * 32 + 32 <= p.d) {
-#pragma unroll
-                for (int u = 0; u < 32; u += 8) {
-                  __align__(16) __half2 hv[4];
-#pragma unroll
-                  for (int w = 0; w < 4; ++w) hv[w] = __floats2half2_rn(v[u + 2 * w], v[u + 2 * w + 1]);
-                  *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
+              for (int q = 0; q < 4; ++q) {
+                if (cc * 32 + q * 8 < p.d) {
+                  const float4 s0 = cs[2 * q], s1 = cs[2 * q + 1], m0 = cm[2 * q], m1 = cm[2 * q + 1];
+                  const float* ov = reinterpret_cast<const float*>(o) + q * 8;
+                  uint4 w;
+                  w.x = pack_out2(fmaf(ov[0] * s0.x, inv_l, m0.x), fmaf(ov[1] * s0.y, inv_l, m0.y), p.dtype);
+                  w.y = pack_out2(fmaf(ov[2] * s0.z, inv_l, m0.z), fmaf(ov[3] * s0.w, inv_l, m0.w), p.dtype);
+                  w.z = pack_out2(fmaf(ov[4] * s1.x, inv_l, m1.x), fmaf(ov[5] * s1.y, inv_l, m1.y), p.dtype);
+                  w.w = pack_out2(fmaf(ov[6] * s1.z, inv_l, m1.z), fmaf(ov[7] * s1.w, inv_l, m1.w), p.dtype);
+                  const int c16 = cc * 4 + q;
+                  if constexpr (kStageOut)
+                    *reinterpret_cast<uint4*>(stage + r * (DP * 2) + ((c16 ^ (r & kSwz)) << 4)) = w;
+                  else
+                    *reinterpret_cast<uint4*>(dst + c16 * 8) = w;
                 }
-              } else {
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                  if (cc * 32 + u < p.d) dst[u] = __float2half_rn(v[u]);
               }
             } else {
-              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + orow + cc * 32;
-              if (p.vec16 && cc * 32 + 32 <= p.d) {
-#pragma unroll
-                for (int u = 0; u < 32; u += 8) {
-                  __align__(16) __nv_bfloat162 hv[4];
-#pragma unroll
-                  for (int w = 0; w < 4; ++w) hv[w] = __floats2bfloat162_rn(v[u + 2 * w], v[u + 2 * w + 1]);
-                  *reinterpret_cast<uint4*>(dst + u) = *reinterpret_cast<const uint4*>(hv);
-                }
-              } else {
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                  if (cc * 32 + u < p.d) dst[u] = __float2bfloat16_rn(v[u]);
+              // element stores: head_dim not a multiple of 8, or unaligned output rows
+#pragma unroll 1
+              for (int u = 0; u < 32 && cc * 32 + u < p.d; ++u) {
+                const int c = cc * 32 + u;
+                const float v = fmaf(__uint_as_float(pick32(o, u)) * __ldg(&vsc[c]), inv_l, __ldg(&vmn[c]));
+                dst[c] = static_cast<uint16_t>(pack_out2(v, 0.f, p.dtype) & 0xffffu);
               }
+            }
+          }
+          if (more) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) { cs[u] = ns[u]; cm[u] = nm[u]; }
+          }
+        }
+        if (kStageOut && vec) {
+          // this warp's 32 staged rows to global memory, whole rows per lane group
+          __syncwarp();
+          const int nch = p.d >> 3;                        // 16-byte chunks of an output row
+          const int lg = (nch & (nch - 1)) == 0 ? __ffs(nch) - 1 : -1;
+          const int r0 = (warp & 3) * 32;
+          const int64_t row_stride = p.o_sn;
+          uint16_t* const dst0 = dst - (int64_t)lane * row_stride;  // row r0 of this warp
+#pragma unroll 1
+          for (int t = lane; t < 32 * nch; t += 32) {
+            const int rr = lg >= 0 ? t >> lg : t / nch;
+            const int c16 = t - rr * nch;
+            const int rw = r0 + rr;
+            if (rw < xrows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * (DP * 2) + ((c16 ^ (rw & kSwz)) << 4));
+              *reinterpret_cast<uint4*>(dst0 + (int64_t)rr * row_stride + c16 * 8) = v;
             }
           }
         }
         if (p.return_lse && row_valid) {
-          float lse = (m + __log2f(l) - log2_sigma) * 0.6931471805599453f;
-          if (p.smooth_k) lse += p.sm_scale * p.qkc[plane_q * p.q_rows + s.row0_q + i];
+          const float lse = (m + __log2f(l) - log2_sigma) * 0.6931471805599453f + p.sm_scale * qk_term;
           const int64_t li = p.varlen ? (int64_t)h * p.lse_plane + s.tok0_q + i
                                       : ((int64_t)b * p.hq + h) * p.nq + i;
           p.lse[li] = lse;
         }
+        trace(p, trs, x, n_tiles - 1, 7);
       }
       if (!ok) record_error(p.err, kDevTimeout);
     }

@@ -153,30 +153,21 @@ constexpr int kRoundMagicBits = 0x4B400000;
 // x * 2^24 split exactly into hi * 2^20 + lo with hi = round(x * 16), lo = (x * 16 - hi) * 2^20.
 // Exact whenever x * 2^24 is an integer and |x| < 2^18 (every fp16 value; bf16 values of
 // magnitude >= 2^-17 or 0): then r = x * 16 - hi is exact and r * 2^20 is an integer < 2^19.
-__device__ __forceinline__ void fixed_split(float x, int& hi, int& lo) {
+// The two words are returned with the rounding constant's bit pattern still in them (hi + and
+// lo + kRoundMagicBits): summing them modulo 2^32 and subtracting n * kRoundMagicBits once
+// gives the sums of n (hi, lo) pairs exactly, as long as those true sums fit in an int32.
+__device__ __forceinline__ void fixed_split_biased(float x, unsigned& hi, unsigned& lo) {
   const float t1 = __fmaf_rn(x, 16.0f, kRoundMagic);
-  hi = __float_as_int(t1) - kRoundMagicBits;
+  hi = __float_as_uint(t1);
   const float r = __fmaf_rn(x, 16.0f, -__fsub_rn(t1, kRoundMagic));
-  lo = __float_as_int(__fmaf_rn(r, 1048576.0f, kRoundMagic)) - kRoundMagicBits;
+  lo = __float_as_uint(__fmaf_rn(r, 1048576.0f, kRoundMagic));
 }
+
 template <typename T>
 __device__ __forceinline__ bool fixed_split_exact(float x) {
   if (std::is_same<T, __half>::value) return true;  // |x| <= 65504, multiples of 2^-24
   const float a = fabsf(x);
   return a < 262144.0f && (a >= 7.62939453125e-06f || a == 0.0f);
-}
-// Adds trunc(x * 2^24) to the (hi, lo, slow) accumulators; values the split cannot take
-// exactly go through the int64 conversion.
-template <typename T>
-__device__ __forceinline__ void fixed_accumulate(float x, int& hi, int& lo, long long& slow) {
-  if (fixed_split_exact<T>(x)) {
-    int h, l;
-    fixed_split(x, h, l);
-    hi += h;
-    lo += l;
-  } else {
-    slow += __float2ll_rz(x * 16777216.0f);
-  }
 }
 
 // Exact, order-free mean from the fixed-point sum: fl32(fl64(fl64(S) * 2^-24 / n)).

@@ -90,16 +90,17 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
       ? static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh
       : static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
   const int64_t sn = KIND == 0 ? p.k_sn : p.v_sn;
-  int hi[8], lo[8];
+  unsigned hi[8], lo[8];  // biased split words, summed modulo 2^32
+  int nrows = 0;           // rows summed by this thread
+  float amax = 0.f;        // max |x| of those rows (range check)
   float mn[8], mx[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    hi[i] = lo[i] = 0;
+    hi[i] = lo[i] = 0u;
     mn[i] = __int_as_float(0x7f800000);
     mx[i] = __int_as_float(0xff800000);
   }
   bool exact = true;  // every value went through the exact int32 split
-  bool range_bad = false;
   if (active) {
     // every row of this thread is requested before any is used
     uint4 raw[kRows];
@@ -114,13 +115,14 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
       if (t0 + rg + RG * r >= t1) continue;
       float x[8];
       unpack8<T>(raw[r], x);
+      ++nrows;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (want_sum) {
-          range_bad |= fabsf(x[i]) >= lim;
+          amax = fmaxf(amax, fabsf(x[i]));
           exact &= fixed_split_exact<T>(x[i]);
-          int h, l;
-          fixed_split(x[i], h, l);
+          unsigned h, l;
+          fixed_split_biased(x[i], h, l);
           hi[i] += h;
           lo[i] += l;
         }
@@ -131,10 +133,13 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
       }
     }
   }
-  if (range_bad) record_error(p.err, kDevRange);
+  if (want_sum && amax >= lim) record_error(p.err, kDevRange);
   long long sum[8];
+  const unsigned bias = static_cast<unsigned>(nrows) * static_cast<unsigned>(kRoundMagicBits);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sum[i] = (static_cast<long long>(hi[i]) << 20) + lo[i];
+  for (int i = 0; i < 8; ++i)
+    sum[i] = (static_cast<long long>(static_cast<int>(hi[i] - bias)) << 20) +
+             static_cast<int>(lo[i] - bias);
   if (!std::is_same<T, __half>::value && want_sum && !__all_sync(0xffffffffu, exact)) {
     // a bf16 value below 2^-17 or above 2^18 in this warp: exact int64 conversion instead
 #pragma unroll

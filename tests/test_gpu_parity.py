@@ -5,7 +5,7 @@ and the integer scores S = Q8·K8^T as the attention kernel reads them from tens
 Tolerance: O within max-abs 2e-2 and cosine >= 0.9995 of the oracle's quantised emulation,
 cosine >= 0.99 of float64 unquantised attention, LSE within 2e-2.
 Cases span several 128-row tiles with ragged tails, both layouts and dtypes, GQA, causal,
-Nq != Nk, head_dim padding (32, 72, 96) and every granularity / accumulation mode.
+Nq != Nk, head_dim padding (32, 40, 72, 96) and every granularity / accumulation mode.
 """
 
 import numpy as np
@@ -37,6 +37,12 @@ CASES = [
     Workload("pad_d96", 1, 2, 2, 257, 129, 96, layout="NHD", gran="per_block", is_causal=True),
     Workload("short_keys", 1, 2, 2, 129, 1, 64, gran="per_warp", smooth_v=True),
     Workload("q_longer_causal", 1, 2, 2, 300, 100, 64, is_causal=True, gran="per_warp"),
+    # head_dim <= 64 rows leave through the staged output path: token-strided (NHD) rows, and
+    # 5 16-byte chunks per row (not a power of two)
+    Workload("nhd_d64_staged", 2, 3, 3, 200, 150, 64, dtype="bf16", layout="NHD", gran="per_warp",
+             accum="fp32", return_lse=True, k_offset_std=2.0),
+    Workload("pad_d40_nhd", 1, 2, 2, 160, 200, 40, layout="NHD", gran="per_block", smooth_v=True,
+             v_offset_std=1.0),
 ]
 
 

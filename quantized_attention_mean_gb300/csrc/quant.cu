@@ -248,9 +248,14 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Threads of a quantisation block: 512 at padded head_dim 128 (16 threads per row, 4 rows each:
+// less unrolled code per warp than 8 rows at 256 threads, and the kernel measured 7-17% faster),
+// 256 at 64 (8 threads per row, 4 rows each; 2 rows each at 512 measured slower).
+__host__ __device__ constexpr int quant_threads(int tpr) { return tpr == 16 ? 512 : 256; }
+
 // Quantisation, one instantiation per tensor (kind 0 = Q, 1 = K, 2 = V). Grid: (128-token
-// tiles, heads, batch). 256 threads; thread (rg, vec) holds rows rg + 16*i (i < 8), channels
-// [8*vec, 8*vec + 8).
+// tiles, heads, batch). quant_threads(TPR) threads; thread (rg, vec) holds rows rg + RG*i
+// (i < 128 / RG, RG = threads / TPR), channels [8*vec, 8*vec + 8).
 //   Q: codes = INT8 per group of gq rows (stored as integer-valued fp16 for the tensor
 //      cores), scales sq, and (return_lse with smooth_k) the LSE term q . kmean.
 //   K: K' = K - kmean, INT8 per group of gk rows.
@@ -260,7 +265,8 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 // Rows past the sequence end up to the stored tile end are written as zeros.
 template <typename T, int kind, int TPR>
 __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, int b) {
-  constexpr int RG = 256 / TPR;      // row groups
+  constexpr int NT = quant_threads(TPR);
+  constexpr int RG = NT / TPR;       // row groups
   constexpr int RPT = kTileRows / RG;  // rows per thread
   const Seq s = get_seq(p, b);
   const int len = kind == 0 ? s.len_q : s.len_k;
@@ -336,7 +342,7 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     const int64_t col0 = (int64_t)s.row0_k + r0;
     const int ncols = (int)min((int64_t)kTileRows, p.vt_pitch - col0);
     __half* vt16 = reinterpret_cast<__half*>(p.vt);
-    for (int idx = threadIdx.x; idx < dp * 16; idx += 256) {
+    for (int idx = threadIdx.x; idx < dp * 16; idx += NT) {
       const int c = idx >> 4, u = idx & 15;  // channel, 8-token unit
       if (u * 8 < ncols) {
         const uint4 val = *reinterpret_cast<const uint4*>(&vtile16[c][(u ^ ((c >> 3) & 15)) << 3]);
@@ -369,7 +375,7 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     const int64_t plane = plane_of(p, b, h, p.hkv);
     const int64_t col0 = (int64_t)s.row0_k + r0;
     const int ncols = (int)min((int64_t)kTileRows, p.vt_pitch - col0);
-    for (int idx = threadIdx.x; idx < dp * 8; idx += 256) {
+    for (int idx = threadIdx.x; idx < dp * 8; idx += NT) {
       const int c = idx >> 3, ch = (idx & 7) * 16;
       if (ch < ncols) {
         uint4 val = *reinterpret_cast<const uint4*>(&vtile[c][ch ^ (((c >> 3) & 7) << 4)]);
@@ -462,7 +468,7 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 // Q, K and V quantisation in one launch. Grid: (128-token tiles of the longest sequence,
 // Hq + 2 Hkv, batch): blockIdx.y selects a Q head, then a K head, then a V head.
 template <typename T, int TPR, bool PV16>
-__global__ void __launch_bounds__(256, TPR == 8 ? 4 : 3) quant_kernel(Problem p) {
+__global__ void __launch_bounds__(quant_threads(TPR), TPR == 8 ? 4 : 2) quant_kernel(Problem p) {
   pdl_trigger();
   pdl_wait();  // the finalisation's means and scales
   const int y = blockIdx.y;
@@ -532,11 +538,11 @@ static cudaError_t launch_quant_t(const Problem& p, int max_len_q, int max_len_k
   const int len = max_len_q > max_len_k ? max_len_q : max_len_k;
   const dim3 grid((len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
   if (p.dp == 64) {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true>, grid, dim3(256), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 8, false>, grid, dim3(256), 0, st, p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true>, grid, dim3(quant_threads(8)), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 8, false>, grid, dim3(quant_threads(8)), 0, st, p);
   } else {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true>, grid, dim3(256), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 16, false>, grid, dim3(256), 0, st, p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true>, grid, dim3(quant_threads(16)), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 16, false>, grid, dim3(quant_threads(16)), 0, st, p);
   }
 }
 

@@ -189,29 +189,44 @@ def cpu_baseline_subprocess(wname, rows):
     return ops, dt
 
 
+def reference_steps(wname, rows, warmup, steps):
+    """Warm-up and timed oracle samples of one workload; returns (ops, seconds) of the timed ones."""
+    from quantized_attention_mean_gb300.workloads import WORKLOADS
+    w = WORKLOADS[wname]
+    for _ in range(warmup):
+        oracle_sample(w, rows)
+    tot_ops, tot_s = 0.0, 0.0
+    for _ in range(steps):
+        ops, dt = oracle_sample(w, rows)
+        tot_ops += ops
+        tot_s += dt
+    return tot_ops, tot_s
+
+
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
         return
     rows = 128
-    for _ in range(args.warmup):
-        oracle_sample(w, rows)
-    tot_ops, tot_s = 0.0, 0.0
-    for _ in range(args.steps):
-        ops, dt = oracle_sample(w, rows)
-        tot_ops += ops
-        tot_s += dt
+    # one single-threaded process (BLAS pinned to 1 thread), so the core count is exact
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench, json; "
+            f"print(json.dumps(bench.reference_steps({w.name!r}, {rows}, {args.warmup}, {args.steps})))")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle process failed: " + r.stderr[-2000:])
+    tot_ops, tot_s = json.loads(r.stdout.strip().splitlines()[-1])
     value = tot_ops / tot_s / 1e12
-    cores = os.cpu_count()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": describe(w), "parallelism": "none (host CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"per step: batch 0 head 0 of {w.name}: K/V/Q quantisation of the head "
-                                   f"+ {rows} of {w.Nq} query rows; numpy (BLAS may thread)"},
+                                   f"+ {rows} of {w.Nq} query rows; numpy, 1 thread (BLAS pinned)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -248,14 +248,12 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Threads of a quantisation block: 512 at padded head_dim 128 (16 threads per row, 4 rows each:
-// less unrolled code per warp than 8 rows at 256 threads, and the kernel measured 7-17% faster),
-// 256 at 64 (8 threads per row, 4 rows each; 2 rows each at 512 measured slower).
-__host__ __device__ constexpr int quant_threads(int tpr) { return tpr == 16 ? 512 : 256; }
-
 // Quantisation, one instantiation per tensor (kind 0 = Q, 1 = K, 2 = V). Grid: (128-token
-// tiles, heads, batch). quant_threads(TPR) threads; thread (rg, vec) holds rows rg + RG*i
-// (i < 128 / RG, RG = threads / TPR), channels [8*vec, 8*vec + 8).
+// tiles, heads, batch). NT threads; thread (rg, vec) holds rows rg + RG*i (i < 128 / RG,
+// RG = NT / TPR), channels [8*vec, 8*vec + 8). NT is 512 for dense problems at padded
+// head_dim 128 (4 rows per thread: less unrolled code per warp than 8 rows at 256 threads,
+// measured 7-17% faster) and 256 otherwise (at head_dim 64, 2 rows per thread measured slower;
+// varlen grids hold many empty tiles, which cost more at 512).
 //   Q: codes = INT8 per group of gq rows (stored as integer-valued fp16 for the tensor
 //      cores), scales sq, and (return_lse with smooth_k) the LSE term q . kmean.
 //   K: K' = K - kmean, INT8 per group of gk rows.
@@ -263,9 +261,8 @@ __host__ __device__ constexpr int quant_threads(int tpr) { return tpr == 16 ? 51
 //      [channel][token] so that P.V reads V^T tiles K-major.
 //   V (kind 3, FP16 P·V variant): V' = V - vmean rounded to fp16 (RNE), transposed likewise.
 // Rows past the sequence end up to the stored tile end are written as zeros.
-template <typename T, int kind, int TPR>
+template <typename T, int kind, int TPR, int NT>
 __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, int b) {
-  constexpr int NT = quant_threads(TPR);
   constexpr int RG = NT / TPR;       // row groups
   constexpr int RPT = kTileRows / RG;  // rows per thread
   const Seq s = get_seq(p, b);
@@ -467,14 +464,14 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 
 // Q, K and V quantisation in one launch. Grid: (128-token tiles of the longest sequence,
 // Hq + 2 Hkv, batch): blockIdx.y selects a Q head, then a K head, then a V head.
-template <typename T, int TPR, bool PV16>
-__global__ void __launch_bounds__(quant_threads(TPR), TPR == 8 ? 4 : 2) quant_kernel(Problem p) {
+template <typename T, int TPR, bool PV16, int NT>
+__global__ void __launch_bounds__(NT, NT == 512 ? 2 : (TPR == 8 ? 4 : 3)) quant_kernel(Problem p) {
   pdl_trigger();
   pdl_wait();  // the finalisation's means and scales
   const int y = blockIdx.y;
-  if (y < p.hq) quant_block<T, 0, TPR>(p, blockIdx.x, y, blockIdx.z);
-  else if (y < p.hq + p.hkv) quant_block<T, 1, TPR>(p, blockIdx.x, y - p.hq, blockIdx.z);
-  else quant_block<T, PV16 ? 3 : 2, TPR>(p, blockIdx.x, y - p.hq - p.hkv, blockIdx.z);
+  if (y < p.hq) quant_block<T, 0, TPR, NT>(p, blockIdx.x, y, blockIdx.z);
+  else if (y < p.hq + p.hkv) quant_block<T, 1, TPR, NT>(p, blockIdx.x, y - p.hq, blockIdx.z);
+  else quant_block<T, PV16 ? 3 : 2, TPR, NT>(p, blockIdx.x, y - p.hq - p.hkv, blockIdx.z);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -538,11 +535,14 @@ static cudaError_t launch_quant_t(const Problem& p, int max_len_q, int max_len_k
   const int len = max_len_q > max_len_k ? max_len_q : max_len_k;
   const dim3 grid((len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
   if (p.dp == 64) {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true>, grid, dim3(quant_threads(8)), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 8, false>, grid, dim3(quant_threads(8)), 0, st, p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true, 256>, grid, dim3(256), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 8, false, 256>, grid, dim3(256), 0, st, p);
+  } else if (!p.varlen) {
+    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true, 512>, grid, dim3(512), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 16, false, 512>, grid, dim3(512), 0, st, p);
   } else {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true>, grid, dim3(quant_threads(16)), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 16, false>, grid, dim3(quant_threads(16)), 0, st, p);
+    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true, 256>, grid, dim3(256), 0, st, p)
+                  : launch_pdl(quant_kernel<T, 16, false, 256>, grid, dim3(256), 0, st, p);
   }
 }
 

@@ -23,6 +23,9 @@ Parity status per function (see the pins in ``tests/test_oracle_*.py``):
   attention.sage_attention               pinned (closed forms: Nk=1, uniform keys, constant V,
                                           causal row 0; quantisation bypass == fp64 attention;
                                           smooth_k invariance; cosine vs fp64)
+  attention online form (p_max="running") pinned (one key tile: identical to the final form;
+                                          codes bypassed: exact attention, causal or not; every
+                                          row's maximum in its first tile: final form to 1e-12)
   attention fp16+fp32 accumulation       parity unpinned beyond the bypass/closed forms: the
                                           in-tile rounding order is a reading, not a definition
   merge.merge_partials                   pinned (chunked fp64 attention merges to the unchunked

@@ -23,6 +23,14 @@ The steps, in the order the method applies them, per (batch, query head):
  10. LSE = m + ln l + sm_scale · (q · k̄)   (natural log; undoes the smooth_k shift)
 Steps 5-10 use library matmuls on exact integer or float64 operands only.
 
+Online form (p_max="running"): the pages' kernel is flash-style (pnsm.cn §2: tiles of keys
+with an online softmax), so P~ can also be read as quantised against the running max of the
+keys seen so far. Steps 6-8 then walk the keys in the same 128-key tiles: per tile, m_new =
+max(m, tile max), α = exp(m - m_new) (0 while m = -inf), p = exp(t - m_new), P~ = e4m3(p · σ_P)
+(fp16 for the FP16 P·V variant), acc = α · acc + P~ · V~ (the fp16+fp32 mode rounds each
+tile's partial to fp16 as above), l = α · l + sum p. Steps 9 and 10 are unchanged. With one
+tile, or when every row's maximum lies in its first tile, the two forms give the same P~.
+
 FP16 P·V variant (pv="fp16"; the guide's §5.3 / §5.4 INT8-QK + FP16-PV kernel, its quality
 fallback with FP8 turned off): step 3 keeps V' as fp16 (RNE) instead of E4M3 with a scale,
 step 7 rounds P to fp16 with σ_P = 1, and step 9 has no V scale. Steps 4-6, 8 and 10 are
@@ -110,7 +118,7 @@ def scores(q8, k8):
 
 
 def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
-                bypass_quant=False, row_chunk=512):
+                bypass_quant=False, row_chunk=512, p_max="final"):
     """Steps 4-10 for one query head against one quantised KV head.
 
     q: float32 [Nq, d] (original values, used for Q quantisation and the LSE term);
@@ -118,8 +126,12 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
     bypass_quant replaces every code by the value it encodes (scales 1, P unrounded):
     the result must then equal exact attention, which pins the non-quantising steps;
     bypass_quant="qk" bypasses only the Q/K codes (P and V keep their P·V format).
+    p_max: "final" (P~ against the row's maximum over all keys) or "running" (the online
+    form: P~ against the maximum of the 128-key tiles seen so far, accumulator rescaled).
     Returns dict(o=float64 [R, d] before output rounding, lse=float64 [R]).
     """
+    if p_max not in ("final", "running"):
+        raise ValueError("p_max must be 'final' or 'running'")
     q = np.asarray(q, np.float32)
     nq, d = q.shape
     nk = kvq["k8"].shape[0]
@@ -166,21 +178,41 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
         t = s * (sq_row[r][:, None] * sk_key[None, :] * sm_scale)  # step 5
         if is_causal:
             t = np.where(keys[None, :] <= r[:, None], t, -np.inf)
-        m = t.max(axis=1)                                  # step 6
-        p = np.exp(t - m[:, None])
-        l = p.sum(axis=1)
-        if bypass_quant is True:                           # step 7
-            pq = p * sig
-        elif pv16:
-            pq = to_fp16(p)
+
+        def quantise_p(p):                                 # step 7
+            if bypass_quant is True:
+                return p * sig
+            if pv16:
+                return to_fp16(p)
+            return e4m3_decode(e4m3_encode(p * sig))
+
+        fp16_tiles = accum == ACC_FP16_FP32 and bypass_quant is not True
+        if p_max == "final":
+            m = t.max(axis=1)                              # step 6
+            p = np.exp(t - m[:, None])
+            l = p.sum(axis=1)
+            pq = quantise_p(p)
+            if fp16_tiles:                                 # step 8
+                acc = np.zeros((len(r), d))
+                for k0 in range(0, nk, PV_TILE):
+                    acc += to_fp16(pq[:, k0:k0 + PV_TILE] @ vd[k0:k0 + PV_TILE])
+            else:
+                acc = pq @ vd
         else:
-            pq = e4m3_decode(e4m3_encode(p * sig))
-        if accum == ACC_FP16_FP32 and bypass_quant is not True:   # step 8
+            # steps 6-8 in the online form, one 128-key tile at a time
+            m = np.full(len(r), -np.inf)
+            l = np.zeros(len(r))
             acc = np.zeros((len(r), d))
             for k0 in range(0, nk, PV_TILE):
-                acc += to_fp16(pq[:, k0:k0 + PV_TILE] @ vd[k0:k0 + PV_TILE])
-        else:
-            acc = pq @ vd
+                tt = t[:, k0:k0 + PV_TILE]
+                m_new = np.maximum(m, tt.max(axis=1))
+                m_ref = np.where(np.isfinite(m_new), m_new, 0.0)
+                alpha = np.exp(m - m_ref)                  # 0 while no key was seen
+                p = np.exp(tt - m_ref[:, None])
+                part = quantise_p(p) @ vd[k0:k0 + PV_TILE]
+                acc = acc * alpha[:, None] + (to_fp16(part) if fp16_tiles else part)
+                l = l * alpha + p.sum(axis=1)
+                m = m_new
         o[c0:c0 + len(r)] = acc * sv[None, :] / (sig * l[:, None]) + vbar[None, :]  # step 9
         lse[c0:c0 + len(r)] = m + np.log(l) + sm_scale * (q[r].astype(np.float64) @ kbar)  # 10
     return dict(o=o, lse=lse)
@@ -196,7 +228,7 @@ def _check_args(hq, hkv, d, accum):
 
 def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WARP,
                    accum=ACC_FP32, smooth_k=True, smooth_v=False, heads=None, rows=None,
-                   bypass_quant=False, pv="fp8"):
+                   bypass_quant=False, pv="fp8", p_max="final"):
     """Dense forward on canonical float32 arrays q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d].
 
     heads: optional list of (b, hq) pairs to compute (default all); rows: optional query
@@ -227,7 +259,7 @@ def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WAR
         qcache[(b, h)] = quantize_q_head(q[b, h], gran)
         res = attend_head(q[b, h], kvcache[key], gran=gran, sm_scale=sm_scale,
                           is_causal=is_causal, accum=accum, rows=rows, qq=qcache[(b, h)],
-                          bypass_quant=bypass_quant)
+                          bypass_quant=bypass_quant, p_max=p_max)
         o[b, h] = res["o"]
         lse[b, h] = res["lse"]
     return dict(o=o, lse=lse, kv=kvcache, q=qcache, sm_scale=sm_scale)

@@ -9,6 +9,16 @@ TOL_MAX_ABS = 2e-2      # O vs the oracle's quantised emulation (max-abs)
 TOL_COS = 0.9995        # O vs the oracle's quantised emulation (cosine)
 TOL_COS_FP64 = 0.99     # O vs float64 unquantised attention (cosine)
 TOL_LSE = 2e-2          # LSE vs the oracle (absolute)
+# O and LSE vs the oracle's online form (p_max="running"), which quantises P~ the way the
+# kernel does. What separates the two is ex2.approx vs exp and fp32 sums; where that tips
+# one P~ across an E4M3 rounding boundary, a row that sees only a few keys moves by up to a
+# few percent of a V value, so the element bound stays at half the bound above while almost
+# every element must agree to 1e-3 (beyond one output ulp), and cosine and LSE are tight.
+TOL_ONLINE_MAX_ABS = 1e-2
+TOL_ONLINE_ELEM = 1e-3
+TOL_ONLINE_ELEM_FRAC = 1e-3
+TOL_ONLINE_COS = 0.99999
+TOL_ONLINE_LSE = 1e-4
 
 
 def out_ulp(x, dtype):
@@ -25,6 +35,21 @@ def max_abs_excess(o_gpu, o_ref, dtype):
     tolerance can round to neighbouring values of that format, so the 2e-2 bound applies on
     top of one ulp."""
     return float(np.max(np.abs(np.asarray(o_gpu, np.float64) - o_ref) - out_ulp(o_ref, dtype)))
+
+
+def excess_fraction(o_gpu, o_ref, dtype, thr):
+    """Fraction of elements whose error beyond one output ulp exceeds thr."""
+    e = np.abs(np.asarray(o_gpu, np.float64) - o_ref) - out_ulp(o_ref, dtype)
+    return float(np.mean(e > thr))
+
+
+def assert_online_parity(o_gpu, o_ref, dtype, lse=None, lse_ref=None):
+    """The output against the oracle's online form (see the TOL_ONLINE_* bounds)."""
+    assert max_abs_excess(o_gpu, o_ref, dtype) <= TOL_ONLINE_MAX_ABS
+    assert excess_fraction(o_gpu, o_ref, dtype, TOL_ONLINE_ELEM) <= TOL_ONLINE_ELEM_FRAC
+    assert cosine(o_gpu, o_ref) >= TOL_ONLINE_COS
+    if lse is not None:
+        assert np.abs(np.asarray(lse) - lse_ref).max() <= TOL_ONLINE_LSE
 
 
 def cosine(a, b):

@@ -8,7 +8,8 @@ import torch
 from oracle.attention import attention_fp64, sage_attention_varlen
 from quantized_attention_mean_gb300.workloads import ACC, GRAN, Workload, varlen_inputs
 
-from helpers import TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, cosine, max_abs_excess
+from helpers import (TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, assert_online_parity, cosine,
+                     max_abs_excess)
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +63,17 @@ def test_varlen_parity(w, lens, pv):
             assert cosine(o[sl, h], of) >= TOL_COS_FP64
     if lse is not None:
         assert np.abs(lse - ref["lse"]).max() <= TOL_LSE
+
+
+@pytest.mark.parametrize("pv", ["fp8", "fp16"])
+@pytest.mark.parametrize("w,lens", CASES, ids=[c[0].name for c in CASES])
+def test_varlen_matches_online_form(w, lens, pv):
+    # per sequence against the oracle's online form (P~ with the running maximum)
+    qn, kn, vn, cu, o, lse, _ = _run(w, lens, pv)
+    ref = sage_attention_varlen(qn, kn, vn, cu, cu, is_causal=w.is_causal, gran=GRAN[w.gran],
+                                accum=ACC[w.accum], smooth_k=w.smooth_k, smooth_v=w.smooth_v,
+                                pv=pv, p_max="running")
+    assert_online_parity(o, ref["o"], w.dtype, lse, ref["lse"])
 
 
 def test_varlen_bad_cu_seqlens_reports_status():

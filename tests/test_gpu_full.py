@@ -14,7 +14,8 @@ from oracle.attention import attend_head, quantize_kv_head, quantize_q_head, sag
 from quantized_attention_mean_gb300.workloads import (ACC, GRAN, WORKLOADS, dense_inputs, to_hnd_f32,
                                                       varlen_inputs)
 
-from helpers import TOL_COS, TOL_LSE, TOL_MAX_ABS, cosine, max_abs_excess, out_to_hnd, run_gpu_dense
+from helpers import (TOL_COS, TOL_LSE, TOL_MAX_ABS, assert_online_parity, cosine, max_abs_excess,
+                     out_to_hnd, run_gpu_dense)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,11 @@ def test_full_size_dense_sampled(name):
         assert cosine(got, ref["o"]) >= TOL_COS
         if lse is not None:
             assert np.abs(lse[b, h, rows] - ref["lse"]).max() <= TOL_LSE
+        # the online form over every key tile of the full sequence
+        onl = attend_head(qn[b, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=w.is_causal,
+                          accum=ACC[w.accum], rows=rows, qq=qq, p_max="running")
+        assert_online_parity(got, onl["o"], w.dtype, lse[b, h, rows] if lse is not None else None,
+                             onl["lse"])
 
 
 def test_full_size_varlen_sampled():
@@ -86,3 +92,6 @@ def test_full_size_varlen_sampled():
             got = o[sl, h][rows]
             assert max_abs_excess(got, ref["o"], w.dtype) <= TOL_MAX_ABS
             assert cosine(got, ref["o"]) >= TOL_COS
+            onl = attend_head(qn[sl, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=False,
+                              accum=ACC[w.accum], rows=rows, p_max="running")
+            assert_online_parity(got, onl["o"], w.dtype)

@@ -351,7 +351,8 @@ def run_ours(args, w):
     fp8_peak = 2.0 * pk["bf16"]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "traffic": ATTN_DRAM_BYTES.get(w.name),
-                "kernel": "attn_kernel<128> (fused QK^T/softmax/PV)",
+                "kernel": f"attn_kernel<{64 if w.d <= 64 else 128}, "
+                          f"{1 if w.extra.get('pv') == 'fp16' else 0}> (fused QK^T/softmax/PV)",
                 "peak_source": f"{pk['src']}: dense FP8 = 2 x bf16 burst {pk['bf16']} TFLOP/s",
                 "route_ceiling_frac": 2.0 / 3.0,
                 "stage_ms_per_step": {"stats": stage_ms[0] / max(calls, 1),

@@ -389,7 +389,8 @@ static int varlen_impl(const sage_packed* q, const sage_packed* k, const sage_pa
     return SAGE_ERR_INVALID_ARG;
   if (batch == 0 || total_q == 0) return SAGE_OK;
   if (total_k == 0 || max_seqlen_k == 0) return SAGE_ERR_INVALID_ARG;
-  if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return SAGE_ERR_INVALID_ARG;
+  if (!cu_seqlens_q || !cu_seqlens_k || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return SAGE_ERR_INVALID_ARG;
   const sage_packed* ts[4] = {q, k, v, out};
   bool vec16 = head_dim % 8 == 0;
   for (const sage_packed* t : ts) {

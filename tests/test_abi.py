@@ -114,3 +114,66 @@ def test_merge_partials_host_validation(lib):
     assert call(out=ctypes.byref(bad)) == 4
     neg = SageTensor(fake, (ctypes.c_int64 * 3)(-64, 64, 64))
     assert call(out=ctypes.byref(neg)) == 4
+
+
+def _varlen(lib, **over):
+    from quantized_attention_mean_gb300._lib import SagePacked
+    fake = 0x10000  # never dereferenced: validation fails or stops before any launch
+    a = dict(qdata=fake, st=2 * 64, sh=64, cuq=fake, cuk=fake, batch=2, maxq=100, maxk=100,
+             tq=150, tk=150, hq=2, hkv=2, d=64, dtype=0, causal=0, scale=0.0, lse=0, gran=1,
+             acc=0, sk=1, sv=0, ws=fake * 16, wsb=1 << 40)
+    a.update(over)
+    t = SagePacked(a["qdata"], a["st"], a["sh"])
+    ok = SagePacked(fake, 2 * 64, 64)
+    return lib.sage_attn_varlen(ctypes.byref(t), ctypes.byref(ok), ctypes.byref(ok), ctypes.byref(ok),
+                                None, ctypes.c_void_p(a["cuq"]), ctypes.c_void_p(a["cuk"]), a["batch"],
+                                a["maxq"], a["maxk"], a["tq"], a["tk"], a["hq"], a["hkv"], a["d"],
+                                a["dtype"], a["causal"], a["scale"], a["lse"], a["gran"], a["acc"],
+                                a["sk"], a["sv"], ctypes.c_void_p(a["ws"]), a["wsb"], None)
+
+
+def test_varlen_host_validation_statuses(lib):
+    assert _varlen(lib, cuq=0) == 1               # null cu_seqlens_q
+    assert _varlen(lib, cuk=0) == 1               # null cu_seqlens_k
+    assert _varlen(lib, cuq=0x10000 + 2) == 1     # cu_seqlens not 4-byte aligned
+    assert _varlen(lib, d=200) == 2               # SAGE_ERR_HEAD_DIM
+    assert _varlen(lib, hq=3) == 5                # SAGE_ERR_GQA
+    assert _varlen(lib, batch=-1) == 1
+    assert _varlen(lib, tq=0) == 0                # no query tokens: no-op
+    assert _varlen(lib, batch=0) == 0
+    assert _varlen(lib, tk=0) == 1                # queries but no keys
+    assert _varlen(lib, maxk=0) == 1
+    assert _varlen(lib, qdata=0) == 1             # null tensor data
+    assert _varlen(lib, qdata=0x10001) == 4       # SAGE_ERR_STRIDE: odd address
+    assert _varlen(lib, st=-128) == 4             # negative token stride
+    assert _varlen(lib, wsb=16) == 6              # SAGE_ERR_WORKSPACE
+    assert _varlen(lib, lse=1) == 1               # return_lse without an lse buffer
+
+
+def test_pv16_entry_host_validation(lib):
+    from quantized_attention_mean_gb300._lib import SageTensor
+    fake = 0x10000
+    t = SageTensor(fake, (ctypes.c_int64 * 3)(2 * 256 * 64, 256 * 64, 64))
+
+    def call(hq=2, hkv=2, d=64, wsb=1 << 40):
+        return lib.sage_attn_qk_int8_pv_fp16(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t),
+                                             ctypes.byref(t), None, 1, hq, hkv, 256, 256, d, 0, 0, 0,
+                                             0.0, 0, 1, 0, 1, 0, ctypes.c_void_p(fake * 16), wsb, None)
+    assert call(d=129) == 2
+    assert call(hq=3) == 5
+    assert call(wsb=16) == 6
+
+
+def test_dense_stride_statuses(lib):
+    from quantized_attention_mean_gb300._lib import SageTensor
+    fake = 0x10000
+    good = SageTensor(fake, (ctypes.c_int64 * 3)(2 * 256 * 64, 256 * 64, 64))
+    odd = SageTensor(fake + 1, (ctypes.c_int64 * 3)(2 * 256 * 64, 256 * 64, 64))
+    neg = SageTensor(fake, (ctypes.c_int64 * 3)(2 * 256 * 64, -256 * 64, 64))
+    for bad in (odd, neg):
+        for pos in range(4):
+            ts = [good] * 4
+            ts[pos] = bad
+            st = lib.sage_attn(*(ctypes.byref(x) for x in ts), None, 1, 2, 2, 256, 256, 64, 0, 0, 0,
+                               0.0, 0, 1, 0, 1, 0, ctypes.c_void_p(fake * 16), 1 << 40, None)
+            assert st == 4, (pos, st)                 # SAGE_ERR_STRIDE

@@ -75,6 +75,38 @@ def alloc_workspace(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def _check_workspace(workspace, device):
+    if workspace is not None and (workspace.dtype != torch.uint8 or workspace.device != device
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+
+
+def _check_dense_args(q, k, v, tensor_layout, out, lse, return_lse, workspace):
+    """Shapes, dtypes and devices of a dense call. The C ABI sees only pointers and strides,
+    so a v smaller than k, or an out / lse smaller than q's, would be read or written past its
+    end: such arguments are rejected here, before anything is launched."""
+    if tensor_layout not in LAYOUT:
+        raise ValueError("tensor_layout must be 'HND' or 'NHD'")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("v must have k's shape")
+    B, Hq, _, Nq, _, d = _dims(q, k, tensor_layout)
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k must have q's batch size and head_dim")
+    if out is not None and (tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype
+                            or out.device != q.device):
+        raise ValueError("out must have q's shape, dtype and device")
+    if return_lse and lse is not None and (tuple(lse.shape) != (B, Hq, Nq) or lse.dtype != torch.float32
+                                           or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor on q's device")
+    if not (q.is_cuda and k.device == q.device and v.device == q.device):
+        raise ValueError("q, k, v must be on one CUDA device")
+    _check_workspace(workspace, q.device)
+
+
 def _dims(q, k, layout):
     if layout == "HND":
         return q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3]
@@ -88,10 +120,7 @@ def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, retu
     k, v: [B, Hkv, Nk, d] / [B, Nk, Hkv, d]; fp16 or bf16 on one CUDA device.
     Returns out (same shape/layout/dtype as q), plus lse [B, Hq, Nq] fp32 if return_lse."""
     lib = _lib.load()
-    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
-    if not (q.is_cuda and k.device == q.device and v.device == q.device):
-        raise ValueError("q, k, v must be on one CUDA device")
+    _check_dense_args(q, k, v, tensor_layout, out, lse, return_lse, workspace)
     B, Hq, Hkv, Nq, Nk, d = _dims(q, k, tensor_layout)
     if out is None:
         out = torch.empty_like(q)
@@ -140,10 +169,28 @@ def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     device. Returns out [Tq, Hq, d] (+ lse [Hq, Tq] fp32 if return_lse). pv="fp16" selects the
     FP16 P·V variant."""
     lib = _lib.load()
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be packed 3-D [tokens, heads, head_dim] tensors")
     if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype, float16 or bfloat16")
+    if tuple(v.shape) != tuple(k.shape) or k.shape[2] != q.shape[2]:
+        raise ValueError("v must have k's shape, and k q's head_dim")
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
+    if (cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape or cu_seqlens_q.numel() < 1
+            or not cu_seqlens_q.is_contiguous() or not cu_seqlens_k.is_contiguous()):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be contiguous 1-D [batch + 1] tensors")
+    if out is not None and (tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype
+                            or out.device != q.device):
+        raise ValueError("out must have q's shape, dtype and device")
+    if return_lse and lse is not None and (tuple(lse.shape) != (q.shape[1], q.shape[0])
+                                           or lse.dtype != torch.float32 or not lse.is_contiguous()
+                                           or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [Hq, total_q] tensor on q's device")
+    if not (q.is_cuda and k.device == q.device and v.device == q.device
+            and cu_seqlens_q.device == q.device and cu_seqlens_k.device == q.device):
+        raise ValueError("q, k, v and cu_seqlens must be on one CUDA device")
+    _check_workspace(workspace, q.device)
     Tq, Hq, d = q.shape
     Tk, Hkv = k.shape[0], k.shape[1]
     B = cu_seqlens_q.numel() - 1
@@ -189,6 +236,14 @@ def merge_partials(outs, lses, tensor_layout="HND", out=None, lse=None, stream=N
     for l in lses:
         if l.dtype != torch.float32 or tuple(l.shape) != (B, H, N) or not l.is_contiguous():
             raise ValueError("each lse must be a contiguous float32 [B, H, N] tensor")
+    if out is not None and (tuple(out.shape) != tuple(o0.shape) or out.dtype != o0.dtype):
+        raise ValueError("out must have the partial outputs' shape and dtype")
+    if lse is not None and (tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    devs = {t.device for t in list(outs) + list(lses) + [x for x in (out, lse) if x is not None]}
+    if len(devs) != 1 or not o0.is_cuda:
+        raise ValueError("all tensors must be on one CUDA device")
     if out is None:
         out = torch.empty_like(o0)
     if lse is None:

@@ -23,7 +23,8 @@ Parity status per function (see the pins in ``tests/test_oracle_*.py``):
   attention.sage_attention               pinned (closed forms: Nk=1, uniform keys, constant V,
                                           causal row 0; quantisation bypass == fp64 attention;
                                           smooth_k invariance; cosine vs fp64)
-  attention online form (p_max="running") pinned (one key tile: identical to the final form;
+  attention online form (p_max="running") pinned (one key tile: identical to the final form,
+                                          FP8 and FP16 P·V; varlen == per-sequence dense;
                                           codes bypassed: exact attention, causal or not; every
                                           row's maximum in its first tile: final form to 1e-12)
   attention fp16+fp32 accumulation       parity unpinned beyond the bypass/closed forms: the

@@ -73,3 +73,34 @@ def test_rejects_unknown_form():
     q = _rand((1, 1, 4, 8), 13)
     with pytest.raises(ValueError):
         sage_attention(q, q, q, p_max="lagging")
+
+
+def test_fp16_pv_variant_online_form():
+    # pv="fp16": one key tile gives the final form's bits; bypassed codes give exact attention
+    q, k, v = _rand((1, 2, 70, 64), 14), _rand((1, 2, 120, 64), 15), _rand((1, 2, 120, 64), 16)
+    a = sage_attention(q, k, v, pv="fp16", p_max="final")
+    b = sage_attention(q, k, v, pv="fp16", p_max="running")
+    np.testing.assert_array_equal(a["o"], b["o"])
+    q, k, v = _rand((1, 1, 150, 32), 17), _rand((1, 1, 300, 32), 18), _rand((1, 1, 300, 32), 19)
+    r = sage_attention(q, k, v, is_causal=True, bypass_quant=True, pv="fp16", p_max="running",
+                       smooth_k=False)
+    o, _ = attention_fp64(q[0, 0], k[0, 0], v[0, 0], r["sm_scale"], True)
+    np.testing.assert_allclose(r["o"][0, 0], o, rtol=0, atol=1e-12)
+
+
+def test_varlen_online_form_equals_per_sequence_dense():
+    from oracle.attention import sage_attention_varlen
+    rng = np.random.default_rng(20)
+    lens = [150, 1, 300]
+    t = sum(lens)
+    q = rng.standard_normal((t, 4, 32)).astype(np.float32)
+    k = rng.standard_normal((t, 2, 32)).astype(np.float32)
+    v = rng.standard_normal((t, 2, 32)).astype(np.float32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    res = sage_attention_varlen(q, k, v, cu, cu, is_causal=True, p_max="running")
+    for b in range(3):
+        sl = slice(cu[b], cu[b + 1])
+        d = sage_attention(q[sl].transpose(1, 0, 2)[None], k[sl].transpose(1, 0, 2)[None],
+                           v[sl].transpose(1, 0, 2)[None], is_causal=True, p_max="running")
+        np.testing.assert_array_equal(res["o"][sl], d["o"][0].transpose(1, 0, 2))
+        np.testing.assert_array_equal(res["lse"][:, sl], d["lse"][0])

@@ -93,9 +93,11 @@ size_t sage_attn_workspace_size(int batch, int heads_q, int heads_kv, int seqlen
  *   sm_scale: scale of the scores; NaN or <= 0 selects 1/sqrt(head_dim).
  *   qk_quant_gran: token groups sharing one INT8 scale — per_block 128 Q rows / 64 K rows,
  *   per_warp 32 / 64, per_thread 1 / 16.
- *   pv_accum_dtype: SAGE_ACC_FP32 or SAGE_ACC_FP32_FP32 (P scaled by 448 before FP8,
- *   fp32 accumulation), SAGE_ACC_FP16_FP32 (P unscaled, each 128-key partial rounded to
- *   fp16 and summed in fp32); SAGE_ACC_FP16 returns SAGE_ERR_UNSUPPORTED.
+ *   pv_accum_dtype: SAGE_ACC_FP32, SAGE_ACC_FP32_FP32 or SAGE_ACC_FP16_FP32, one
+ *   arithmetic on this GPU: P is scaled by 448 before its FP8 rounding and P·V accumulates
+ *   in fp32 over every key (§4.2 ranks fp16 accumulation fastest and fp32 most stable, with
+ *   fp16+fp32 between them; the tensor cores here accumulate fp16 no faster than fp32, so the
+ *   compromise is taken at fp32); SAGE_ACC_FP16 returns SAGE_ERR_UNSUPPORTED.
  *   smooth_k / smooth_v: subtract the per-(batch, head, channel) mean over the sequence.
  *   Nq == 0 or B == 0 is a no-op returning SAGE_OK.
  * Returns a sage_status. */
@@ -111,8 +113,8 @@ int sage_attn(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
  * arguments, workspace size and errors, except that V' = V - v̄ is kept in fp16 (no per-channel
  * scale) and P = 2^(t - m) is rounded to fp16 (σ_P = 1); both P·V operands are fp16 on the
  * tensor cores (kind::f16) with fp32 accumulation. pv_accum_dtype: SAGE_ACC_FP32,
- * SAGE_ACC_FP32_FP32 or SAGE_ACC_FP16_FP32 (all accumulate in fp32); SAGE_ACC_FP16 returns
- * SAGE_ERR_UNSUPPORTED. |V - v̄| beyond the fp16 range becomes ±inf. */
+ * SAGE_ACC_FP32_FP32 or SAGE_ACC_FP16_FP32 (one arithmetic, as for sage_attn);
+ * SAGE_ACC_FP16 returns SAGE_ERR_UNSUPPORTED. |V - v̄| beyond the fp16 range becomes ±inf. */
 int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                               const sage_tensor* out, float* lse, int batch, int heads_q,
                               int heads_kv, int seqlen_q, int seqlen_k, int head_dim, int dtype,
@@ -134,8 +136,11 @@ int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const 
  *   Arguments, layouts and results are those of sage_attn.
  *   Returns SAGE_ERR_WORKSPACE, before launching anything, when the problem needs more than
  *   SAGE_NO_ALLOC_SCRATCH_BYTES of scratch (sage_attn_workspace_size tells how much).
+ *   Arguments are checked first, with sage_attn's rules and error codes.
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current); make that first call before any stream capture.
+ *   with that device current) and caches it for the life of the process; make that first
+ *   call before any stream capture. After a cudaDeviceReset the cached address is stale:
+ *   do not call this entry point in a process that has reset a device it used.
  *   Every call on a device uses the same array: calls that may overlap on the GPU (other
  *   streams, other host threads) race and must be serialised by the caller. Each call
  *   clears what it needs cleared; nothing an earlier call left in the array is read.

@@ -4,7 +4,8 @@ This package is a plain, slow, obviously-correct restatement of what the GPU pat
 computes, written from the method's description (pwwt.cn "SageAttention deployment
 pitfalls guide", §1 "why attention is the bottleneck" for the three-stage idea, §4.1/§4.2
 for the API knobs qk_quant_gran / pv_accum_dtype / smooth_k / smooth_v, §4 for
-sageattn_varlen) plus the readings listed in the design doc where the pages are silent.
+sageattn_varlen), with a stated reading wherever the guide is silent; each module's docstring
+names the readings it takes.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl
 reference`` legs of ``bench.py`` may import it. The product path
@@ -27,8 +28,10 @@ Parity status per function (see the pins in ``tests/test_oracle_*.py``):
                                           FP8 and FP16 P·V; varlen == per-sequence dense;
                                           codes bypassed: exact attention, causal or not; every
                                           row's maximum in its first tile: final form to 1e-12)
-  attention fp16+fp32 accumulation       parity unpinned beyond the bypass/closed forms: the
-                                          in-tile rounding order is a reading, not a definition
+  accumulation modes                     pinned (fp16+fp32, fp32+fp32 and fp32 are one
+                                          arithmetic, σ_P = 448: a two-key case worked by hand
+                                          from the E4M3 table, identical-key and single-key
+                                          closed forms in every mode)
   merge.merge_partials                   pinned (chunked fp64 attention merges to the unchunked
                                           result; empty parts; single part; order invariance)
 """

@@ -6,7 +6,8 @@ pwwt.cn "SageAttention deployment pitfalls guide":
   §4.1 sageattn(q, k, v, tensor_layout, is_causal, sm_scale=None -> 1/sqrt(head_dim),
        return_lse); head_dim padding rule; GQA (Hq divisible by Hkv); Nq may differ
        from Nk;
-  §4.2 pv_accum_dtype in {fp16, fp32, fp16+fp32};
+  §4.2 pv_accum_dtype in {fp16, fp32, fp16+fp32}: all-fp16 fastest but may be unstable,
+       fp32 the most stable, fp16+fp32 a compromise between the two;
   §4 (end) sageattn_varlen with cu_seqlens_q / cu_seqlens_k.
 
 The steps, in the order the method applies them, per (batch, query head):
@@ -16,25 +17,29 @@ The steps, in the order the method applies them, per (batch, query head):
   4. S = Q8 · K8^T, exact integers
   5. t = S · s_q · s_k · sm_scale, causal mask (key j allowed iff j <= i), in float64
   6. m = row max of t (final max), p = exp(t - m), l = sum p
-  7. P~ = e4m3(p · σ_P), σ_P = 448 (fp32 accumulation) or 1 (fp16+fp32)
-  8. acc = P~ · V~ (fp32 modes: float64 sum; fp16+fp32: each 128-key tile's partial
-     rounded to fp16 before the float64 sum)
+  7. P~ = e4m3(p · σ_P), σ_P = 448 (the largest E4M3 magnitude)
+  8. acc = P~ · V~ as a float64 sum
   9. O = acc · s_v / (σ_P · l) + v̄, rounded once to the output dtype
  10. LSE = m + ln l + sm_scale · (q · k̄)   (natural log; undoes the smooth_k shift)
 Steps 5-10 use library matmuls on exact integer or float64 operands only.
+
+Accumulation modes (§4.2): the guide ranks fp16 accumulation as the fastest and fp32 as the
+most stable, with fp16+fp32 as the compromise; it gives no other arithmetic for them. On the
+tensor cores this library targets an fp16 accumulator is not faster than an fp32 one, so the
+compromise costs nothing to resolve in fp32's favour: "fp16+fp32", "fp32+fp32" and "fp32" are
+one arithmetic here (σ_P = 448, one sum over every key), and pure "fp16" is not supported.
 
 Online form (p_max="running"): the pages' kernel is flash-style (pnsm.cn §2: tiles of keys
 with an online softmax), so P~ can also be read as quantised against the running max of the
 keys seen so far. Steps 6-8 then walk the keys in the same 128-key tiles: per tile, m_new =
 max(m, tile max), α = exp(m - m_new) (0 while m = -inf), p = exp(t - m_new), P~ = e4m3(p · σ_P)
-(fp16 for the FP16 P·V variant), acc = α · acc + P~ · V~ (the fp16+fp32 mode rounds each
-tile's partial to fp16 as above), l = α · l + sum p. Steps 9 and 10 are unchanged. With one
+(fp16 for the FP16 P·V variant), acc = α · acc + P~ · V~, l = α · l + sum p. Steps 9 and 10 are unchanged. With one
 tile, or when every row's maximum lies in its first tile, the two forms give the same P~.
 
 FP16 P·V variant (pv="fp16"; the guide's §5.3 / §5.4 INT8-QK + FP16-PV kernel, its quality
 fallback with FP8 turned off): step 3 keeps V' as fp16 (RNE) instead of E4M3 with a scale,
 step 7 rounds P to fp16 with σ_P = 1, and step 9 has no V scale. Steps 4-6, 8 and 10 are
-unchanged (the fp16+fp32 mode keeps its per-tile fp16 rounding).
+unchanged.
 """
 
 import numpy as np
@@ -44,7 +49,7 @@ from .quant import (GRAN_PER_BLOCK, GRAN_PER_THREAD, GRAN_PER_WARP, K_GROUP, Q_G
                     fixed_point_mean, fp8_channel_quant, int8_group_quant, smooth)
 
 ACC_FP32, ACC_FP16_FP32, ACC_FP32_FP32, ACC_FP16 = 0, 1, 2, 3
-PV_TILE = 128  # keys per P·V tile for the fp16+fp32 in-tile rounding
+KEY_TILE = 128  # keys per tile of the online form
 
 __all__ = [
     "ACC_FP32", "ACC_FP16_FP32", "ACC_FP32_FP32", "ACC_FP16", "GRAN_PER_BLOCK",
@@ -60,9 +65,12 @@ def default_sm_scale(head_dim):
 
 
 def sigma_p(accum):
+    """Scale of P before its E4M3 rounding: 448 in every supported accumulation mode."""
     if accum == ACC_FP16:
         raise NotImplementedError("pure fp16 P·V accumulation is not supported")
-    return 1.0 if accum == ACC_FP16_FP32 else 448.0
+    if accum not in (ACC_FP32, ACC_FP16_FP32, ACC_FP32_FP32):
+        raise ValueError("unknown accumulation mode")
+    return 448.0
 
 
 def round_float(x, sig_bits, min_normal_exp, max_finite):
@@ -137,9 +145,9 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
     nk = kvq["k8"].shape[0]
     rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
     pv16 = kvq.get("pv") == "fp16"
-    sig = 1.0 if pv16 else sigma_p(accum)
-    if accum == ACC_FP16:
-        sigma_p(accum)  # raises: pure fp16 accumulation is not supported
+    sig = sigma_p(accum)       # raises for pure fp16 accumulation or an unknown mode
+    if pv16:
+        sig = 1.0              # fp16 P needs no scaling into its format's range
     if bypass_quant is True:
         qv = q.astype(np.float64)
         sq_row = np.ones(nq)
@@ -186,31 +194,23 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
                 return to_fp16(p)
             return e4m3_decode(e4m3_encode(p * sig))
 
-        fp16_tiles = accum == ACC_FP16_FP32 and bypass_quant is not True
         if p_max == "final":
             m = t.max(axis=1)                              # step 6
             p = np.exp(t - m[:, None])
             l = p.sum(axis=1)
-            pq = quantise_p(p)
-            if fp16_tiles:                                 # step 8
-                acc = np.zeros((len(r), d))
-                for k0 in range(0, nk, PV_TILE):
-                    acc += to_fp16(pq[:, k0:k0 + PV_TILE] @ vd[k0:k0 + PV_TILE])
-            else:
-                acc = pq @ vd
+            acc = quantise_p(p) @ vd                       # steps 7-8
         else:
             # steps 6-8 in the online form, one 128-key tile at a time
             m = np.full(len(r), -np.inf)
             l = np.zeros(len(r))
             acc = np.zeros((len(r), d))
-            for k0 in range(0, nk, PV_TILE):
-                tt = t[:, k0:k0 + PV_TILE]
+            for k0 in range(0, nk, KEY_TILE):
+                tt = t[:, k0:k0 + KEY_TILE]
                 m_new = np.maximum(m, tt.max(axis=1))
                 m_ref = np.where(np.isfinite(m_new), m_new, 0.0)
                 alpha = np.exp(m - m_ref)                  # 0 while no key was seen
                 p = np.exp(tt - m_ref[:, None])
-                part = quantise_p(p) @ vd[k0:k0 + PV_TILE]
-                acc = acc * alpha[:, None] + (to_fp16(part) if fp16_tiles else part)
+                acc = acc * alpha[:, None] + quantise_p(p) @ vd[k0:k0 + KEY_TILE]
                 l = l * alpha + p.sum(axis=1)
                 m = m_new
         o[c0:c0 + len(r)] = acc * sv[None, :] / (sig * l[:, None]) + vbar[None, :]  # step 9

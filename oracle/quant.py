@@ -8,10 +8,11 @@ Follows pwwt.cn "SageAttention deployment pitfalls guide":
 and pnsm.cn "SageAttention on AMD 9070 XT without the HIP SDK" §2 (split into small
 blocks, take each block's range, compress to 8 bits).
 
-The pages give no group sizes, rounding rule or summation order; the readings used here
-(token groups of 128/32/1 for Q and 64/64/16 for K, scale = absmax/127 with a reciprocal
-multiply and ties-to-even rounding, an order-free fixed-point mean) are listed in
-DESIGN.md. Everything is per (batch, head) — or per (sequence, head) for varlen.
+The pages give no group sizes, rounding rule or summation order. The readings taken here:
+token groups of 128/32/1 rows for Q and 64/64/16 rows for K (per_block / per_warp /
+per_thread), restarting per sequence; scale = absmax/127 with codes from a reciprocal
+multiply and ties-to-even rounding; an order-free fixed-point mean. Everything is per
+(batch, head) — or per (sequence, head) for varlen.
 """
 
 import numpy as np

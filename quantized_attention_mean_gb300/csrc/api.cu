@@ -191,7 +191,6 @@ void fill_common(Problem& p, const Common& c) {
   p.return_lse = c.return_lse ? 1 : 0;
   p.smooth_k = c.smooth_k ? 1 : 0;
   p.smooth_v = c.smooth_v ? 1 : 0;
-  p.acc_mode = c.acc == SAGE_ACC_FP16_FP32 ? 1 : 0;
   p.sm_scale = (std::isnan(c.sm_scale) || c.sm_scale <= 0.f)
                    ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.d)))
                    : c.sm_scale;
@@ -314,6 +313,9 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
 }
 
 }  // namespace
+
+int note_cuda_failure(cudaError_t e, const char* where) { return cuda_fail(e, where); }
+
 }  // namespace sage
 
 using namespace sage;

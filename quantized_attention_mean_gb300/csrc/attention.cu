@@ -458,8 +458,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const bool active_tile = x == 0 || has_b;
     const int i = q_start + x * kTileRows + r;  // query row within the sequence
     const bool row_valid = active_tile && r < xrows;
-    // sigma_P: 448 for E4M3 P in the fp32 modes, 1 for fp16+fp32 and for fp16 P
-    const float log2_sigma = (PV16 || p.acc_mode == 1) ? 0.0f : 8.807354922057604f;  // log2(448)
+    // sigma_P: 448 (the largest E4M3 magnitude) for E4M3 P in every accumulation mode, 1 for
+    // fp16 P
+    const float log2_sigma = PV16 ? 0.0f : 8.807354922057604f;  // log2(448)
     const bool trs = tr && (warp & 3) == 0 && lane == 0;
     float sq = 0.f;
     if (row_valid) sq = __ldg(&p.sq[plane_q * p.sq_pp + (s.row0_q + i) / p.gq]);

@@ -23,6 +23,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Records a failed CUDA call for sage_last_cuda_error (calling thread) and returns
+// SAGE_ERR_CUDA.
+int note_cuda_failure(cudaError_t e, const char* where);
+
 cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st);
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st);
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st);

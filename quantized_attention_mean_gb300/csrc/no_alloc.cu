@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/sageattn.h"
+#include "launch.h"
 
 namespace {
 
@@ -24,14 +25,26 @@ void* g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
 
 // Device address of the scratch array on the current device. In host code g_scratch names
 // a host-side stand-in, so the address is looked up once per device (with that device
-// current) and cached. Returns nullptr if the lookup fails.
+// current) and cached. On failure the runtime's error is taken off the thread (so that no
+// later launch check reports it as its own) and recorded for sage_last_cuda_error;
+// returns nullptr.
 void* scratch_address() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    sage::note_cuda_failure(e != cudaSuccess ? e : cudaErrorInvalidDevice, "no-alloc scratch: device");
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess) return nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      sage::note_cuda_failure(e, "no-alloc scratch: cudaGetSymbolAddress");
+      return nullptr;
+    }
     g_scratch_addr[dev] = ptr;
   }
   return g_scratch_addr[dev];
@@ -45,9 +58,17 @@ extern "C" int sage_attn_no_alloc(const sage_tensor* q, const sage_tensor* k, co
                                   int dtype, int tensor_layout, int is_causal, float sm_scale,
                                   int return_lse, int qk_quant_gran, int pv_accum_dtype,
                                   int smooth_k, int smooth_v, void* stream) {
+  // Argument checks first, with sage_attn's own rules and codes: without a workspace it
+  // validates everything else and launches nothing (an empty problem returns SAGE_OK, a
+  // valid one SAGE_ERR_WORKSPACE).
+  const int st = sage_attn(q, k, v, out, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k,
+                           head_dim, dtype, tensor_layout, is_causal, sm_scale, return_lse,
+                           qk_quant_gran, pv_accum_dtype, smooth_k, smooth_v, nullptr, 0, stream);
+  if (st != SAGE_ERR_WORKSPACE) return st;
   const size_t need = sage_attn_workspace_size(batch, heads_q, heads_kv, seqlen_q, seqlen_k,
                                                head_dim, qk_quant_gran);
   if (need > SAGE_NO_ALLOC_SCRATCH_BYTES) return SAGE_ERR_WORKSPACE;
+  if (!sage_device_supported()) return SAGE_ERR_DEVICE;
   void* scratch = scratch_address();
   if (scratch == nullptr) return SAGE_ERR_CUDA;
   // The statistics and status regions are cleared by the call itself; nothing left in the

@@ -24,7 +24,6 @@ struct Problem {
   int nq, nk;                      // dense: sequence lengths; varlen: max lengths
   int varlen, dtype, is_causal, return_lse, smooth_k, smooth_v;
   int gq, gk, lgk;                 // token-group sizes of Q and K scales; lgk = log2(gk)
-  int acc_mode;                    // 0: fp32 (P scaled by 448), 1: fp16 partials + fp32
   int vec16;                       // inputs allow 16-byte vector loads
   int pv16;                        // FP16 P·V variant: V^T stored as fp16, P in fp16
   float sm_scale;

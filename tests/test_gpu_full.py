@@ -1,5 +1,7 @@
-"""Full-size workloads, in the launch configuration bench.py times, checked on sampled query
-rows (the oracle computes those rows one by one) and sampled heads' quantised tensors.
+"""Full-size workloads, in the launch configuration bench.py times: every head's quantised
+tensors (INT8 Q / K codes and scales, E4M3 V codes and scales, the smoothing means) bit for
+bit, and sampled query rows of three heads against the oracle's attention (which computes
+those rows one by one).
 
 Workloads: 4K self-attention (2x8x4096^2, d=128, fp16+fp32), causal GQA decoder (1x32/8x8192^2,
 bf16 NHD, per_thread, LSE), video-DiT long sequence (2x48x17776^2, d=64, biased K/V,
@@ -38,20 +40,37 @@ def test_full_size_dense_sampled(name):
     o = out_to_hnd(g["out"], w.layout)
     assert np.isfinite(o).all()
     lse = g["lse"].cpu().numpy() if w.return_lse else None
-    ex = qa.export_quant(g["ws"], w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran)
-    rows = _rows(w.Nq)
+    ex = {n: t.cpu().numpy() for n, t in
+          qa.export_quant(g["ws"], w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran).items()}
     grp = w.Hq // w.Hkv
+    gran = GRAN[w.gran]
+    # every head's quantised tensors, bit for bit: K / V codes, scales and means per KV head,
+    # Q codes and scales per query head
+    rows = _rows(w.Nq)
     heads = [(0, 0), (w.B - 1, w.Hq - 1), (0, w.Hq // 2 + 1)]
+    kvq_keep = {}
+    for b in range(w.B):
+        for hk in range(w.Hkv):
+            kvq = quantize_kv_head(kn[b, hk], vn[b, hk], gran, w.smooth_k, w.smooth_v)
+            np.testing.assert_array_equal(ex["k8"][b, hk], kvq["k8"])
+            np.testing.assert_array_equal(ex["v8"][b, hk], kvq["v8"])
+            np.testing.assert_array_equal(ex["sk"][b, hk].view(np.uint32), kvq["sk"].view(np.uint32))
+            np.testing.assert_array_equal(ex["vscale"][b, hk].view(np.uint32), kvq["sv"].view(np.uint32))
+            np.testing.assert_array_equal(ex["kmean"][b, hk].view(np.uint32), kvq["kbar"].view(np.uint32))
+            np.testing.assert_array_equal(ex["vmean"][b, hk].view(np.uint32), kvq["vbar"].view(np.uint32))
+            if any((b, hk) == (hb, hh // grp) for hb, hh in heads):
+                kvq_keep[(b, hk)] = kvq
+        for h in range(w.Hq):
+            qq = quantize_q_head(qn[b, h], gran)
+            np.testing.assert_array_equal(ex["q8"][b, h], qq["q8"])
+            np.testing.assert_array_equal(ex["sq"][b, h].view(np.uint32), qq["sq"].view(np.uint32))
+    del ex
+    # sampled rows of three heads against the oracle's attention
     sm = default_sm_scale(w.d)
     for (b, h) in heads:
-        kvq = quantize_kv_head(kn[b, h // grp], vn[b, h // grp], GRAN[w.gran], w.smooth_k, w.smooth_v)
-        qq = quantize_q_head(qn[b, h], GRAN[w.gran])
-        np.testing.assert_array_equal(ex["q8"][b, h].cpu().numpy(), qq["q8"])
-        np.testing.assert_array_equal(ex["k8"][b, h // grp].cpu().numpy(), kvq["k8"])
-        np.testing.assert_array_equal(ex["v8"][b, h // grp].cpu().numpy(), kvq["v8"])
-        np.testing.assert_array_equal(ex["sk"][b, h // grp].cpu().numpy().view(np.uint32), kvq["sk"].view(np.uint32))
-        np.testing.assert_array_equal(ex["sq"][b, h].cpu().numpy().view(np.uint32), qq["sq"].view(np.uint32))
-        ref = attend_head(qn[b, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=w.is_causal,
+        kvq = kvq_keep[(b, h // grp)]
+        qq = quantize_q_head(qn[b, h], gran)
+        ref = attend_head(qn[b, h], kvq, gran=gran, sm_scale=sm, is_causal=w.is_causal,
                           accum=ACC[w.accum], rows=rows, qq=qq)
         got = o[b, h, rows]
         assert max_abs_excess(got, ref["o"], w.dtype) <= TOL_MAX_ABS
@@ -59,7 +78,7 @@ def test_full_size_dense_sampled(name):
         if lse is not None:
             assert np.abs(lse[b, h, rows] - ref["lse"]).max() <= TOL_LSE
         # the online form over every key tile of the full sequence
-        onl = attend_head(qn[b, h], kvq, gran=GRAN[w.gran], sm_scale=sm, is_causal=w.is_causal,
+        onl = attend_head(qn[b, h], kvq, gran=gran, sm_scale=sm, is_causal=w.is_causal,
                           accum=ACC[w.accum], rows=rows, qq=qq, p_max="running")
         assert_online_parity(got, onl["o"], w.dtype, lse[b, h, rows] if lse is not None else None,
                              onl["lse"])

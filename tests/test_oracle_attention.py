@@ -105,9 +105,8 @@ def test_identical_keys_give_uniform_weights():
     assert np.all(kv["k8"] == 0)                 # K - mean(K) = 0 exactly
     expect = e4m3_decode(kv["v8"]).mean(axis=0) * kv["sv"]
     np.testing.assert_allclose(res["o"][0, 0], np.broadcast_to(expect, (17, 32)), rtol=1e-12, atol=1e-12)
-    # fp16+fp32: each 128-key tile partial is rounded to fp16 (relative 2^-11 per tile)
     res16 = sage_attention(q, k, v, accum=ACC_FP16_FP32, smooth_k=True)
-    np.testing.assert_allclose(res16["o"][0, 0], np.broadcast_to(expect, (17, 32)), rtol=2e-3, atol=1e-3)
+    np.testing.assert_allclose(res16["o"][0, 0], np.broadcast_to(expect, (17, 32)), rtol=1e-12, atol=1e-12)
 
 
 def test_constant_v_with_smooth_v_gives_mean():
@@ -230,3 +229,46 @@ def test_output_rounding_helpers():
     assert to_bf16(np.float64(1.0 + 3 * 2.0**-8)) == 1.0 + 2.0**-6
     x = np.random.default_rng(39).standard_normal(1000)
     np.testing.assert_array_equal(to_fp16(x), x.astype(np.float16).astype(np.float64))
+
+
+def _e4m3_nearest(x):
+    """Round a positive real to the E4M3 grid by scanning the stored value table (nearest,
+    ties to the even code), independently of the oracle's encoder."""
+    import os
+    from fractions import Fraction
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e4m3_positive_values.txt")
+    vals = []
+    with open(path) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                c, v = ln.split()
+                vals.append((float(Fraction(v)), int(c, 16)))
+    best = min(vals, key=lambda t: (abs(t[0] - x), t[1] & 1))
+    return best[0]
+
+
+@pytest.mark.parametrize("accum", [ACC_FP32, ACC_FP16_FP32])
+def test_two_keys_closed_form(accum):
+    # head_dim 1, one query, two keys: every quantisation step can be done by hand.
+    #   q = 1 -> code 127, s_q = fl32(1/127);  k = (1, 0.5) -> one K group, codes (127, 64)
+    #   (0.5 * fl32(127) = 63.5 rounds to even 64), s_k = fl32(1/127); scores 16129 and 8128;
+    #   v = (2, -1) -> s_v = fl32(2/448), codes 448 and -224 (both exact in E4M3).
+    # With sm_scale = 10: t_j = S_j s_q s_k 10, p2 = exp(t2 - t1) ~ 0.0070; every accumulation
+    # mode scales P by 448 before its E4M3 rounding: P~ = (448, e4m3(448 p2)), l = 1 + p2
+    # (unquantised), O = (P~1 V~1 + P~2 V~2) s_v / (448 l), LSE = t1 + ln l.
+    q = np.float32([[[[1.0]]]])
+    k = np.float32([[[[1.0], [0.5]]]])
+    v = np.float32([[[[2.0], [-1.0]]]])
+    res = sage_attention(q, k, v, sm_scale=10.0, gran=GRAN_PER_THREAD, accum=accum, smooth_k=False)
+    kv, qq = res["kv"][(0, 0)], res["q"][(0, 0)]
+    assert qq["q8"].ravel().tolist() == [127] and kv["k8"].ravel().tolist() == [127, 64]
+    s_qk = float(np.float32(1.0) / np.float32(127.0))
+    s_v = float(np.float32(2.0) / np.float32(448.0))
+    t1, t2 = 16129.0 * s_qk * s_qk * 10.0, 8128.0 * s_qk * s_qk * 10.0
+    p2 = np.exp(t2 - t1)
+    pt2 = _e4m3_nearest(448.0 * p2)
+    assert pt2 != _e4m3_nearest(p2) * 448.0          # the scale of P is visible here
+    l = 1.0 + p2
+    o = (448.0 * 448.0 + pt2 * -224.0) * s_v / (448.0 * l)
+    np.testing.assert_allclose(res["o"][0, 0, 0, 0], o, rtol=1e-14)
+    np.testing.assert_allclose(res["lse"][0, 0, 0], t1 + np.log(l), rtol=1e-14)

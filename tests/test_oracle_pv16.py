@@ -33,8 +33,8 @@ def test_constant_v_with_smoothing_is_exact():
 @pytest.mark.parametrize("accum", [ACC_FP32, ACC_FP16_FP32])
 def test_pv_rounding_within_fp16_bound(accum):
     # Q/K codes bypassed: what remains is fp16 rounding of P (values <= 1) and of V'; each is
-    # a relative error <= 2^-11 (plus 2^-25 absolute for subnormal P), and the fp16+fp32
-    # mode adds one fp16 rounding of each 128-key partial
+    # a relative error <= 2^-11 (plus 2^-25 absolute for subnormal P) in every
+    # accumulation mode
     q, k, v = _rand(3, 33, 300, 64, scale=1.3)
     kvq = quantize_kv_head(k, v, GRAN_PER_THREAD, True, True, pv="fp16")
     o = attend_head(q, kvq, gran=GRAN_PER_THREAD, sm_scale=0.125, is_causal=False, accum=accum,
@@ -43,8 +43,6 @@ def test_pv_rounding_within_fp16_bound(accum):
     o_exact = o_exact + kvq["vbar"].astype(np.float64)
     vmax = float(np.abs(kvq["v_smoothed"]).max())
     bound = 2.0 ** -10 * 1.01 * vmax + 300 * 2.0 ** -25 * vmax
-    if accum == ACC_FP16_FP32:
-        bound += 3 * 2.0 ** -11 * vmax        # three partials, each |partial| / l <= vmax
     assert np.max(np.abs(o - o_exact)) <= bound
 
 

@@ -5,18 +5,17 @@ library instead of a caller workspace. This file is collected last, so a run tha
 its first failure has already run every other test.
 
 Checked through the C ABI against sage_attn on two calls in a row (different sizes and
-options, so a stale scratch from the first call would show), with the tolerance the other
-parity tests use, and the size limit's error."""
+options, so a stale scratch from the first call would show). Both run the same kernels on the
+same inputs and the pipeline is deterministic (integer statistics sums, fixed launch order), so
+the outputs and LSE must agree bit for bit; and the size limit's error."""
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from quantized_attention_mean_gb300.workloads import Workload, dense_inputs
 
-from helpers import TOL_COS, TOL_MAX_ABS, cosine, max_abs_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -54,13 +53,10 @@ def test_no_alloc_matches_sage_attn_on_consecutive_calls():
         lse = torch.full((w.B, w.Hq, w.Nq), float("nan"), device=dev) if w.return_lse else None
         assert _no_alloc(lib, q, k, v, out, lse, w) == 0
         torch.cuda.synchronize()
-        a = ref_o.float().cpu().numpy()
-        b = out.float().cpu().numpy()
-        assert np.isfinite(b).all()
-        assert max_abs_excess(b, a, w.dtype) <= TOL_MAX_ABS
-        assert cosine(b, a) >= TOL_COS
+        assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref_o)
         if lse is not None:
-            assert np.abs(lse.cpu().numpy() - ref_l.cpu().numpy()).max() <= 2e-2
+            assert torch.equal(lse, ref_l)
 
 
 def test_no_alloc_rejects_problems_beyond_its_scratch():

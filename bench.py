@@ -1,17 +1,22 @@
 """Benchmark: quantized attention TOPS (4·B·H·Nq·Nk·d / s, halved for causal) on GB300.
 
 One step = one full sage_attn call (K/V statistics + quantisation + fused attention) on one
-batch of synthetic inputs of the 4K self-attention workload (B=2, H=8, Nq=Nk=4096, d=128,
-fp16, HND, non-causal, per_warp INT8 Q/K, smooth_k, FP8 V, fp16+fp32 P.V accumulation).
-Inputs rotate over several resident sets whose footprint exceeds the 129 MB L2, so no step
-starts with its inputs cached.
+batch of synthetic inputs. The default workload is the video-DiT-shaped long sequence (B=2,
+H=48, Nq=Nk=17776, d=64, bf16, HND, non-causal, per_warp INT8 Q/K, smooth_k and smooth_v,
+FP8 V, fp16+fp32 P.V accumulation): the largest single-GPU configuration, on which the metric
+is quoted. Its inputs (3 x 208 MiB) exceed the 129 MB L2, and every workload rotates over
+enough resident input sets that one pass over them exceeds L2, so no step starts with its
+inputs cached.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--windows R] [--impl ours|reference]
+                  [--workload NAME]
 
+The K timed steps are one window bracketed by a barrier and a device synchronisation; the
+window is repeated R times (default 25) and the median window gives ms_per_step and value.
 Under torchrun each rank runs the same per-GPU workload (weak scaling, no collective on the
 data path); rank 0 prints one JSON line with the max time over ranks.
-`--impl reference` times the CPU oracle (the slow, plain restatement of the method) on a
-bounded sample of the same workload.
+`--impl reference` times the CPU oracle (the slow, plain restatement of the method) on the
+host cores, on a bounded sample of the same workload per step.
 """
 
 import argparse
@@ -29,22 +34,40 @@ METRIC = "quantized attention TOPS (4·B·H·Nq·Nk·d/s) at 1 GB300; % of INT8/
 UNIT = "TOPS"
 L2_BYTES = 129 * 2**20
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, from the ncu
-# capture summarised in profiles/ (same kernel source); None where no capture exists. Must be
-# cleared whenever the attention kernel changes.
-ATTN_DRAM_BYTES = {"sdpa4k": 42_117_888}
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch of a workload,
+# from the ncu captures summarised in profiles/ (a smaller case of the same kernel scaled to the
+# full launch by the units processed where the full size is too large to capture), with the
+# SHA-256 of the attention kernel's source at capture time: the figure is reported only while
+# the source is unchanged.
+ATTN_DRAM_BYTES = {}
+
+
+def attention_source_digest():
+    import hashlib
+    path = os.path.join(ROOT, "quantized_attention_mean_gb300", "csrc", "attention.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(wname):
+    entry = ATTN_DRAM_BYTES.get(wname)
+    if entry is None or entry[1] != attention_source_digest():
+        return None
+    return entry[0]
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--windows", type=int, default=25,
+                    help="timed windows of --steps steps each; the median window is reported")
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
                     help="timed loop: replay one captured CUDA graph per input set (default), or "
                          "call the API directly each step")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="sdpa4k")
+    ap.add_argument("--workload", default="dit17776")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -165,65 +188,121 @@ def parse_clock_samples(text):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, rows, seed=0):
-    """Times the oracle on one (batch 0, head 0) slice: that head's K/V and Q quantisation and
-    `rows` query rows of attention. Returns (ops, seconds)."""
+def host_cpu():
+    """(logical cores, CPU model string) of this host."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in ln:
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model == "unknown":
+        import platform
+        model = platform.processor() or platform.machine()
+    return os.cpu_count() or 1, model
+
+
+def save_heads(w, heads, directory, seed=0):
+    """Writes the float32 Q / K / V of the given (batch, query head) pairs of the workload's
+    seeded inputs (the same tensors the GPU arm uses) to directory/head_<b>_<h>.npz."""
     import numpy as np
-    from oracle.attention import attend_head, quantize_kv_head, quantize_q_head, default_sm_scale
-    from quantized_attention_mean_gb300.workloads import ACC, GRAN, dense_inputs, to_hnd_f32
+    from quantized_attention_mean_gb300.workloads import dense_inputs, to_hnd_f32
     q, k, v = dense_inputs(w, seed)
     qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
+    grp = w.Hq // w.Hkv
+    paths = []
+    for (b, h) in heads:
+        path = os.path.join(directory, f"head_{b}_{h}.npz")
+        np.savez(path, q=qn[b, h], k=kn[b, h // grp], v=vn[b, h // grp])
+        paths.append(path)
+    return paths
+
+
+def oracle_rows(path, r0, r1, wname):
+    """One oracle worker: quantises one head (K/V statistics, Q/K/V quantisation) and computes
+    attention for query rows [r0, r1). Returns (ops, t_start, t_end) with the ops counted as
+    the metric counts them (4·rows·Nk·d, halved for causal)."""
+    import numpy as np
+    from oracle.attention import attend_head, default_sm_scale, quantize_kv_head, quantize_q_head
+    from quantized_attention_mean_gb300.workloads import ACC, GRAN, WORKLOADS
+    w = WORKLOADS[wname]
+    z = np.load(path)
+    q, k, v = z["q"], z["k"], z["v"]
     g = GRAN[w.gran]
     t0 = time.perf_counter()
-    kvq = quantize_kv_head(kn[0, 0], vn[0, 0], g, w.smooth_k, w.smooth_v, pv=w.extra.get("pv", "fp8"))
-    qq = quantize_q_head(qn[0, 0], g)
-    attend_head(qn[0, 0], kvq, gran=g, sm_scale=default_sm_scale(w.d), is_causal=w.is_causal,
-                accum=ACC[w.accum], rows=np.arange(rows), qq=qq)
-    dt = time.perf_counter() - t0
-    ops = 4.0 * rows * w.Nk * w.d / (2.0 if w.is_causal else 1.0)
-    return ops, dt
+    kvq = quantize_kv_head(k, v, g, w.smooth_k, w.smooth_v, pv=w.extra.get("pv", "fp8"))
+    qq = quantize_q_head(q, g)
+    attend_head(q, kvq, gran=g, sm_scale=default_sm_scale(w.d), is_causal=w.is_causal,
+                accum=ACC[w.accum], rows=np.arange(r0, r1), qq=qq)
+    t1 = time.perf_counter()
+    ops = 4.0 * (r1 - r0) * k.shape[0] * w.d / (2.0 if w.is_causal else 1.0)
+    return ops, t0, t1
 
 
-def cpu_baseline_subprocess(wname, rows):
-    """Runs the oracle sample in a fresh single-threaded process (BLAS pinned to 1 thread)."""
+def run_oracle_workers(jobs, wname):
+    """Runs one single-threaded oracle process per job (path, r0, r1) at once, on the host
+    cores, and returns (ops, seconds): all jobs' ops over the span from the first start to the
+    last end (each process times its own work, after its imports)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench, json; "
-            f"from quantized_attention_mean_gb300.workloads import WORKLOADS; "
-            f"print(json.dumps(bench.oracle_sample(WORKLOADS[{wname!r}], {rows})))")
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
-    ops, dt = json.loads(r.stdout.strip().splitlines()[-1])
-    return ops, dt
+    procs = []
+    for path, r0, r1 in jobs:
+        code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+                f"print(json.dumps(bench.oracle_rows({path!r}, {r0}, {r1}, {wname!r})))")
+        procs.append(subprocess.Popen([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    res = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=1800)
+        if pr.returncode != 0:
+            raise RuntimeError("oracle worker failed: " + err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    ops = sum(r[0] for r in res)
+    return ops, max(r[2] for r in res) - min(r[1] for r in res)
 
 
-def reference_steps(wname, rows, warmup, steps):
-    """Warm-up and timed oracle samples of one workload; returns (ops, seconds) of the timed ones."""
-    from quantized_attention_mean_gb300.workloads import WORKLOADS
-    w = WORKLOADS[wname]
-    for _ in range(warmup):
-        oracle_sample(w, rows)
-    tot_ops, tot_s = 0.0, 0.0
-    for _ in range(steps):
-        ops, dt = oracle_sample(w, rows)
-        tot_ops += ops
-        tot_s += dt
-    return tot_ops, tot_s
+def cpu_baseline_whole_head(w, directory, cores):
+    """The oracle on one whole head (batch 0, head 0) at full size, its query rows split over
+    all host cores (each process also quantises the head, as the oracle does)."""
+    (path,) = save_heads(w, [(0, 0)], directory)
+    n = max(1, min(cores, w.Nq))
+    cuts = [w.Nq * i // n for i in range(n + 1)]
+    return run_oracle_workers([(path, cuts[i], cuts[i + 1]) for i in range(n)], w.name)
+
+
+def reference_rows(w):
+    """Query rows per worker and step of the reference arm: about 0.3-1 s of oracle work."""
+    return max(32, min(w.Nq, int(4e9 / (4.0 * w.Nk * w.d))))
 
 
 def run_reference(args, w):
+    import shutil
+    import tempfile
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
         return
-    rows = 128
-    # one single-threaded process (BLAS pinned to 1 thread), so the core count is exact
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench, json; "
-            f"print(json.dumps(bench.reference_steps({w.name!r}, {rows}, {args.warmup}, {args.steps})))")
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
-    if r.returncode != 0:
-        raise RuntimeError("oracle process failed: " + r.stderr[-2000:])
-    tot_ops, tot_s = json.loads(r.stdout.strip().splitlines()[-1])
+    if w.varlen:
+        raise SystemExit("the reference arm times dense workloads")
+    cores, model = host_cpu()
+    heads = [(i // w.Hq % w.B, i % w.Hq) for i in range(min(cores, w.B * w.Hq))]
+    rows = reference_rows(w)
+    tmp = tempfile.mkdtemp(prefix="sage_oracle_")
+    try:
+        paths = save_heads(w, heads, tmp)
+        jobs = [(p, 0, rows) for p in paths]
+        for _ in range(args.warmup):
+            run_oracle_workers(jobs, w.name)
+        tot_ops, tot_s = 0.0, 0.0
+        for _ in range(args.steps):
+            ops, sec = run_oracle_workers(jobs, w.name)
+            tot_ops += ops
+            tot_s += sec
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
     value = tot_ops / tot_s / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
@@ -231,9 +310,12 @@ def run_reference(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": describe(w), "parallelism": "none (host CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"per step: batch 0 head 0 of {w.name}: K/V/Q quantisation of the head "
-                                   f"+ {rows} of {w.Nq} query rows; numpy, 1 thread (BLAS pinned)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(jobs), "cpu_model": model,
+                         "kind": "oracle",
+                         "sample": f"per step: {len(jobs)} single-threaded processes at once, each "
+                                   f"quantising one head of {w.name} (K/V statistics, Q/K/V "
+                                   f"quantisation) and attending {rows} of its {w.Nq} query rows; "
+                                   f"numpy, BLAS pinned to 1 thread per process"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -322,23 +404,29 @@ def run_ours(args, w):
     assert qa.read_device_status(sets[0][5]) == 0
 
     ops = w.ops(lens) if w.varlen else w.ops()
+    n_windows = max(1, args.windows)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
-    barrier(ws_n, dev)
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        run(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws_n, dev)
-    elapsed_ms = e0.elapsed_time(e1)
+    window_ms = []
+    i0 = 0
+    for _ in range(n_windows):
+        barrier(ws_n, dev)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            run(i0 + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n, dev)
+        window_ms.append(e0.elapsed_time(e1))
+        i0 += args.steps
+    median_ms = statistics.median(window_ms)
     # per-kernel timing: the same steps again with the library's stage events, which keep
     # consecutive kernels from overlapping (programmatic dependent launch), so the throughput
     # above is taken without them
-    n_prof = min(args.steps, 200)
+    n_prof = max(args.steps, min(200, args.steps * n_windows))
     qa.profile_enable(True)
     for i in range(n_prof):
         step(i)
@@ -346,31 +434,55 @@ def run_ours(args, w):
     stage_ms, calls = qa.profile_read()
     qa.profile_enable(False)
     clocks = sampler.stop()
-    for s in sets:
-        assert qa.read_device_status(s[5]) == 0
-    max_s = max_over_ranks(elapsed_ms / 1e3, ws_n, dev)
+    for s_ in sets:
+        assert qa.read_device_status(s_[5]) == 0
+    max_s = max_over_ranks(median_ms / 1e3, ws_n, dev)
     value = aggregate(ops, args.steps, max_s, ws_n)
 
     # roofline of the dominant kernel (the fused attention kernel): algorithmic ops per launch
-    # over its mean event-timed duration. Peak: dense FP8 = measured bf16 burst x 2 (QK^T runs
-    # at the fp16 rate, P.V at FP8: route ceiling 2/3 of it); the FP16 P.V variant runs both
-    # products at the fp16 rate, so its peak is the fp16 (= bf16) one itself.
-    attn_ms = stage_ms[2] / max(calls, 1)
+    # over its mean event-timed duration. Peak: dense FP8 = measured bf16 x 2 (QK^T runs at the
+    # fp16 rate, P.V at FP8: route ceiling 2/3 of it); the FP16 P.V variant runs both products
+    # at the fp16 rate, so its peak is the fp16 (= bf16) one itself. The burst peak is the
+    # reported denominator; the sustained one (seconds-long loop under the power cap) beside it.
+    per = max(calls, 1)
+    attn_ms = stage_ms[2] / per
     achieved = ops / (attn_ms / 1e3) / 1e12
     pv16 = w.extra.get("pv") == "fp16"
     fp8_peak = 2.0 * pk["bf16"]
     kpeak = pk["bf16"] if pv16 else fp8_peak
+    kpeak_sust = pk["bf16_sust"] if pv16 else 2.0 * pk["bf16_sust"]
+    # pre-pass (statistics + quantisation): HBM-bound; algorithmic bytes 3 per element of Q, K
+    # and V (2 read, 1 written as an 8-bit code); the bytes the kernels move with the codes
+    # in their fp16 carrier are reported beside them
+    if w.varlen:
+        n_q = q0.shape[0] * w.Hq * w.d
+        n_kv = k0.shape[0] * w.Hkv * w.d
+    else:
+        n_q = w.B * w.Hq * w.Nq * w.d
+        n_kv = w.B * w.Hkv * w.Nk * w.d
+    alg_bytes = 3 * (n_q + 2 * n_kv)
+    moved = (2 * n_kv * (2 if w.smooth_k else 1)      # statistics: V (and K) read
+             + 4 * n_q + 4 * n_kv                        # Q, K: 2 read + 2 written
+             + n_kv * (4 if pv16 else 3))                # V: 2 read + 1 (fp16 variant: 2) written
+    pre_ms = (stage_ms[0] + stage_ms[1]) / per
+    pre_gbs = alg_bytes / (pre_ms / 1e3) / 1e9
     roofline = {"bound": "tensor", "achieved": achieved, "peak": kpeak, "unit": "TFLOP/s",
-                "frac": achieved / kpeak, "traffic": ATTN_DRAM_BYTES.get(w.name),
+                "frac": achieved / kpeak, "traffic": measured_traffic(w.name),
                 "kernel": f"attn_kernel<{64 if w.d <= 64 else 128}, {1 if pv16 else 0}> "
                           "(fused QK^T/softmax/PV)",
                 "peak_source": (f"{pk['src']}: dense fp16 = bf16 burst {pk['bf16']} TFLOP/s" if pv16 else
                                 f"{pk['src']}: dense FP8 = 2 x bf16 burst {pk['bf16']} TFLOP/s"),
+                "peak_sustained": kpeak_sust, "frac_of_sustained": achieved / kpeak_sust,
                 "route_ceiling_frac": 1.0 if pv16 else 2.0 / 3.0,
-                "stage_ms_per_step": {"stats": stage_ms[0] / max(calls, 1),
-                                      "quant": stage_ms[1] / max(calls, 1), "attention": attn_ms},
+                "algorithmic_ops_per_launch": ops,
+                "prepass": {"bound": "hbm", "achieved": pre_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                            "frac": pre_gbs / pk["hbm"], "algorithmic_bytes": alg_bytes,
+                            "bytes_moved_fp16_carrier": moved,
+                            "kernels": "kv_stats_kernel + kv_finalize_kernel + quant_kernel"},
+                "stage_ms_per_step": {"stats": stage_ms[0] / per, "quant": stage_ms[1] / per,
+                                      "attention": attn_ms},
                 "stage_timing": f"CUDA events around each stage over {calls} steps run right "
-                                "after the timed region (same inputs and launches)"}
+                                "after the timed windows (same inputs and launches)"}
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -438,16 +550,26 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline and not w.varlen:
-        rows = w.Nq  # one full head
-        c_ops, c_s = cpu_baseline_subprocess(w.name, rows)
-        cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"batch 0 head 0 of {w.name}: that head's K/V/Q quantisation + {rows} of "
-                         f"{w.Nq} query rows ({c_ops:.3g} ops in {c_s:.1f} s, 1 thread)"}
+        import shutil
+        import tempfile
+        cores, model = host_cpu()
+        tmp = tempfile.mkdtemp(prefix="sage_oracle_")
+        try:
+            c_ops, c_s = cpu_baseline_whole_head(w, tmp, cores)
+        finally:
+            shutil.rmtree(tmp, ignore_errors=True)
+        n_proc = max(1, min(cores, w.Nq))
+        cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": n_proc, "cpu_model": model,
+               "kind": "oracle",
+               "sample": f"one whole head (batch 0, head 0) of {w.name} at full size: its {w.Nq} "
+                         f"query rows split over {n_proc} single-threaded processes, each also "
+                         f"quantising the head ({c_ops:.3g} ops in {c_s:.1f} s)"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+            "windows": {"count": n_windows, "statistic": "median", "ms": [round(x, 4) for x in window_ms]},
             "scaling": "weak", "vs_baseline": None, "dtype": "int8 QK (exact, fp16 carrier) + " + ("fp16" if w.extra.get("pv") == "fp16" else "e4m3") + " PV, fp32 softmax",
             "data": "synthetic",
             "config": {"workload": describe(w), "parallelism": f"replicas x{ws_n} (independent heads/batches)",
@@ -460,7 +582,7 @@ def run_ours(args, w):
             "e2e": e2e,
             # K/V statistics, their finalisation, Q/K/V quantisation, attention (+ varlen
             # set-up); the clear of the status and statistics is a cudaMemsetAsync
-            "gpu_launches": (5 if w.varlen else 4) * args.steps,
+            "gpu_launches": (5 if w.varlen else 4) * args.steps * n_windows,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -68,6 +68,11 @@ WORKLOADS = {
     # the 4K self-attention shape on the FP16 P·V variant
     "sdpa4k_pv16": Workload("sdpa4k_pv16", 2, 8, 8, 4096, 4096, 128, gran="per_warp",
                             accum="fp16+fp32", extra={"pv": "fp16"}),
+    # half the heads of the DiT shape at batch 1 (same per-CTA work): a profiling case whose
+    # attention launch is short enough for a multi-pass ncu capture
+    "dit17776_h24": Workload("dit17776_h24", 1, 24, 24, 17776, 17776, 64, dtype="bf16",
+                             gran="per_warp", accum="fp16+fp32", smooth_v=True, k_offset_std=4.0,
+                             v_offset_std=2.0),
     "varlen16": Workload("varlen16", 16, 32, 32, 0, 0, 128, gran="per_warp", accum="fp32",
                          varlen=True, n_seqs=16),
 }

@@ -1,5 +1,7 @@
 """bench.py --impl reference on the host CPU: one JSON line with the contract's keys, the
-oracle timed single-threaded (cores == 1), its own value repeated as cpu_baseline and e2e."""
+oracle timed in one single-threaded process per sampled head on the host cores (as many as the
+host has, at most one per head of the workload), its own value repeated as cpu_baseline and
+e2e."""
 
 import json
 import os
@@ -22,7 +24,8 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference"
     assert line["steps"] == 2 and line["warmup"] == 3
     assert line["value"] > 0 and line["higher_is_better"] is True
-    assert line["cpu_baseline"]["cores"] == 1 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == min(os.cpu_count(), 2)   # tiny: B*H = 2 heads
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cpu_model"]
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}

@@ -360,10 +360,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
    } else if (warp == 9) {
     // =========================================================== MMA issuer
-    // one thread issues both query tiles' MMAs, alternating A and B, so the two tiles' softmax
-    // phases stay offset by half an iteration and the tensor core serves one while the other
-    // computes
-    if (lane == 0) {
+    // The whole warp runs the issue loop converged and one elected lane issues each MMA and
+    // commit (warp-uniform operands). Both query tiles' MMAs are issued alternating A and B,
+    // so the two tiles' softmax phases stay offset by half an iteration and the tensor core
+    // serves one while the other computes.
+    {
+      const bool tr_mma = tr && lane == 0;
       const int nx = has_b ? 2 : 1;
       // descriptor bases; a K step inside a 128-byte row adds its byte offset / 16 to the
       // start-address field (no carry: shared-memory addresses stay below 2^18)
@@ -371,6 +373,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t dk = sdesc_sw128(smem_u32(sK));
       const uint64_t dp = sdesc_sw128(smem_u32(sP));
       const uint64_t dv = sdesc_sw128(smem_u32(sV));
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
       auto issue_qk = [&](int x, int st) {
         const uint32_t d_s = tmem + (x ? 128u : 0u);
         const uint64_t qx = dq + static_cast<uint64_t>((x * C::kQTileBytes) >> 4);
@@ -378,9 +383,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int k = 0; k < DP / 16; ++k) {
           const uint32_t off = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
-          mma_f16_ss(d_s, qx + off, kst + off, idesc_qk(), k > 0);
+          mma_f16_ss_warp(d_s, qx + off, kst + off, idesc_qk(), k > 0);
         }
-        mma_commit(&s_full[x]);
+        mma_commit_warp(&s_full[x]);
       };
       auto issue_pv = [&](int x, int sv, int buf, bool first) {
         const uint32_t d_o = tmem + (x ? 384u : 256u);
@@ -393,56 +398,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int k = 0; k < kTileKeys / 16; ++k) {
             const uint32_t op = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
             const uint32_t ov = ((k >> 2) * (DP * 128) + (k & 3) * 32) >> 4;
-            mma_f16_ss(d_o, px + op, vst + ov, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+            mma_f16_ss_warp(d_o, px + op, vst + ov, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
           }
         } else {
 #pragma unroll
           for (int k = 0; k < kTileKeys / 32; ++k)
-            mma_f8_ss(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+            mma_f8_ss_warp(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
         }
-        mma_commit(&o_full[x]);
+        mma_commit_warp(&o_full[x]);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(&k_full[0], 0, abort_flag);
+      bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < nx; ++x) issue_qk(x, 0);
-        mma_commit(&k_empty[0]);
+        mma_commit_warp(&k_empty[0]);
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int sv = j % C::kVStages;
         const int nst = (j + 1) % C::kKStages;
         for (int x = 0; x < nx && ok; ++x) {
           // S_j(x) consumed and P_j(x) written: the tile's next scores can start right away
-          ok = mbar_wait(&p_full[x], j & 1, abort_flag);
+          ok = wait_all(&p_full[x], j & 1);
           if (!ok) break;
-          trace(p, tr, 2, j, 4 * x + 0);
+          trace(p, tr_mma, 2, j, 4 * x + 0);
           tc_fence_after();
           if (j + 1 < n_tiles) {
-            if (x == 0) ok = mbar_wait(&k_full[nst], ((j + 1) / C::kKStages) & 1, abort_flag);
+            if (x == 0) ok = wait_all(&k_full[nst], ((j + 1) / C::kKStages) & 1);
             if (!ok) break;
             tc_fence_after();
             issue_qk(x, nst);
           }
-          trace(p, tr, 2, j, 4 * x + 1);
+          trace(p, tr_mma, 2, j, 4 * x + 1);
           // O(x) rescaled for the new running max: accumulate P_j(x) V_j
-          ok = mbar_wait(&o_ready[x], j & 1, abort_flag);
+          ok = wait_all(&o_ready[x], j & 1);
           if (!ok) break;
-          trace(p, tr, 2, j, 4 * x + 2);
-          if (x == 0) ok = mbar_wait(&v_full[sv], (j / C::kVStages) & 1, abort_flag);
+          trace(p, tr_mma, 2, j, 4 * x + 2);
+          if (x == 0) ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_pv(x, sv, j % C::kPBufs, j == 0);
-          trace(p, tr, 2, j, 4 * x + 3);
+          trace(p, tr_mma, 2, j, 4 * x + 3);
         }
         if (!ok) break;
-        if (j + 1 < n_tiles) mma_commit(&k_empty[nst]);
-        mma_commit(&v_empty[sv]);
+        if (j + 1 < n_tiles) mma_commit_warp(&k_empty[nst]);
+        mma_commit_warp(&v_empty[sv]);
       }
       // every MMA must have finished before tensor memory is released
-      mma_commit(&drain[0]);
+      mma_commit_warp(&drain[0]);
       volatile int never = 0;
       mbar_wait(&drain[0], 0, &never);
-      if (!ok) record_error(p.err, kDevTimeout);
+      __syncwarp();
+      if (!ok && lane == 0) record_error(p.err, kDevTimeout);
     }
    }
   } else {

@@ -31,10 +31,12 @@ one arithmetic here (σ_P = 448, one sum over every key), and pure "fp16" is not
 
 Online form (p_max="running"): the pages' kernel is flash-style (pnsm.cn §2: tiles of keys
 with an online softmax), so P~ can also be read as quantised against the running max of the
-keys seen so far. Steps 6-8 then walk the keys in the same 128-key tiles: per tile, m_new =
-max(m, tile max), α = exp(m - m_new) (0 while m = -inf), p = exp(t - m_new), P~ = e4m3(p · σ_P)
-(fp16 for the FP16 P·V variant), acc = α · acc + P~ · V~, l = α · l + sum p. Steps 9 and 10 are unchanged. With one
-tile, or when every row's maximum lies in its first tile, the two forms give the same P~.
+keys seen so far. Steps 6-8 then walk the keys in tiles of `key_tile` keys (default 128;
+the width is the kernel's choice, so it is a parameter here): per tile, m_new = max(m, tile
+max), α = exp(m - m_new) (0 while m = -inf), p = exp(t - m_new), P~ = e4m3(p · σ_P) (fp16 for
+the FP16 P·V variant), acc = α · acc + P~ · V~, l = α · l + sum p. Steps 9 and 10 are
+unchanged. With one tile, or when every row's maximum lies in its first tile, the two forms
+give the same P~.
 
 FP16 P·V variant (pv="fp16"; the guide's §5.3 / §5.4 INT8-QK + FP16-PV kernel, its quality
 fallback with FP8 turned off): step 3 keeps V' as fp16 (RNE) instead of E4M3 with a scale,
@@ -49,7 +51,7 @@ from .quant import (GRAN_PER_BLOCK, GRAN_PER_THREAD, GRAN_PER_WARP, K_GROUP, Q_G
                     fixed_point_mean, fp8_channel_quant, int8_group_quant, smooth)
 
 ACC_FP32, ACC_FP16_FP32, ACC_FP32_FP32, ACC_FP16 = 0, 1, 2, 3
-KEY_TILE = 128  # keys per tile of the online form
+KEY_TILE = 128  # default keys per tile of the online form
 
 __all__ = [
     "ACC_FP32", "ACC_FP16_FP32", "ACC_FP32_FP32", "ACC_FP16", "GRAN_PER_BLOCK",
@@ -126,7 +128,7 @@ def scores(q8, k8):
 
 
 def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
-                bypass_quant=False, row_chunk=512, p_max="final"):
+                bypass_quant=False, row_chunk=512, p_max="final", key_tile=KEY_TILE):
     """Steps 4-10 for one query head against one quantised KV head.
 
     q: float32 [Nq, d] (original values, used for Q quantisation and the LSE term);
@@ -135,11 +137,14 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
     the result must then equal exact attention, which pins the non-quantising steps;
     bypass_quant="qk" bypasses only the Q/K codes (P and V keep their P·V format).
     p_max: "final" (P~ against the row's maximum over all keys) or "running" (the online
-    form: P~ against the maximum of the 128-key tiles seen so far, accumulator rescaled).
+    form: P~ against the maximum of the key tiles seen so far, accumulator rescaled);
+    key_tile: keys per tile of the online form.
     Returns dict(o=float64 [R, d] before output rounding, lse=float64 [R]).
     """
     if p_max not in ("final", "running"):
         raise ValueError("p_max must be 'final' or 'running'")
+    if key_tile < 1:
+        raise ValueError("key_tile must be positive")
     q = np.asarray(q, np.float32)
     nq, d = q.shape
     nk = kvq["k8"].shape[0]
@@ -204,13 +209,13 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
             m = np.full(len(r), -np.inf)
             l = np.zeros(len(r))
             acc = np.zeros((len(r), d))
-            for k0 in range(0, nk, KEY_TILE):
-                tt = t[:, k0:k0 + KEY_TILE]
+            for k0 in range(0, nk, key_tile):
+                tt = t[:, k0:k0 + key_tile]
                 m_new = np.maximum(m, tt.max(axis=1))
                 m_ref = np.where(np.isfinite(m_new), m_new, 0.0)
                 alpha = np.exp(m - m_ref)                  # 0 while no key was seen
                 p = np.exp(tt - m_ref[:, None])
-                acc = acc * alpha[:, None] + quantise_p(p) @ vd[k0:k0 + KEY_TILE]
+                acc = acc * alpha[:, None] + quantise_p(p) @ vd[k0:k0 + key_tile]
                 l = l * alpha + p.sum(axis=1)
                 m = m_new
         o[c0:c0 + len(r)] = acc * sv[None, :] / (sig * l[:, None]) + vbar[None, :]  # step 9
@@ -228,7 +233,7 @@ def _check_args(hq, hkv, d, accum):
 
 def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WARP,
                    accum=ACC_FP32, smooth_k=True, smooth_v=False, heads=None, rows=None,
-                   bypass_quant=False, pv="fp8", p_max="final"):
+                   bypass_quant=False, pv="fp8", p_max="final", key_tile=KEY_TILE):
     """Dense forward on canonical float32 arrays q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d].
 
     heads: optional list of (b, hq) pairs to compute (default all); rows: optional query
@@ -259,7 +264,7 @@ def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WAR
         qcache[(b, h)] = quantize_q_head(q[b, h], gran)
         res = attend_head(q[b, h], kvcache[key], gran=gran, sm_scale=sm_scale,
                           is_causal=is_causal, accum=accum, rows=rows, qq=qcache[(b, h)],
-                          bypass_quant=bypass_quant, p_max=p_max)
+                          bypass_quant=bypass_quant, p_max=p_max, key_tile=key_tile)
         o[b, h] = res["o"]
         lse[b, h] = res["lse"]
     return dict(o=o, lse=lse, kv=kvcache, q=qcache, sm_scale=sm_scale)

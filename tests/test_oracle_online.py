@@ -20,27 +20,31 @@ def _rand(shape, seed, scale=1.0):
     return (np.random.default_rng(seed).standard_normal(shape) * scale).astype(np.float32)
 
 
-def test_single_tile_forms_identical():
-    q, k, v = _rand((1, 2, 90, 64), 1), _rand((1, 2, 128, 64), 2), _rand((1, 2, 128, 64), 3)
+@pytest.mark.parametrize("key_tile", [96, 128])
+def test_single_tile_forms_identical(key_tile):
+    nk = key_tile
+    q, k, v = _rand((1, 2, 90, 64), 1), _rand((1, 2, nk, 64), 2), _rand((1, 2, nk, 64), 3)
     for accum in (ACC_FP32, ACC_FP16_FP32):
         a = sage_attention(q, k, v, accum=accum, p_max="final")
-        b = sage_attention(q, k, v, accum=accum, p_max="running")
+        b = sage_attention(q, k, v, accum=accum, p_max="running", key_tile=key_tile)
         np.testing.assert_array_equal(a["o"], b["o"])
         np.testing.assert_array_equal(a["lse"], b["lse"])
 
 
+@pytest.mark.parametrize("key_tile", [96, 128, 7])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bypassed_codes_give_exact_attention(causal):
+def test_bypassed_codes_give_exact_attention(causal, key_tile):
     q, k, v = _rand((1, 1, 200, 32), 4), _rand((1, 1, 333, 32), 5), _rand((1, 1, 333, 32), 6)
     r = sage_attention(q, k, v, is_causal=causal, bypass_quant=True, p_max="running",
-                       smooth_k=False)
+                       smooth_k=False, key_tile=key_tile)
     o, lse = attention_fp64(q[0, 0], k[0, 0], v[0, 0], r["sm_scale"], causal)
     np.testing.assert_allclose(r["o"][0, 0], o, rtol=0, atol=1e-12)
     np.testing.assert_allclose(r["lse"][0, 0], lse, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("key_tile", [96, 128])
 @pytest.mark.parametrize("accum", [ACC_FP32, ACC_FP16_FP32])
-def test_maximum_in_first_tile_matches_final_form(accum):
+def test_maximum_in_first_tile_matches_final_form(accum, key_tile):
     # positive queries and a positive first key: key 0 has every row's largest score (by ~7
     # natural-log units), while the other keys keep non-zero E4M3 probabilities
     q = np.abs(_rand((1, 2, 64, 64), 7)) + 0.1
@@ -48,7 +52,8 @@ def test_maximum_in_first_tile_matches_final_form(accum):
     k[:, :, 0, :] = 1.5
     v = _rand((1, 2, 400, 64), 9)
     a = sage_attention(q, k, v, accum=accum, gran=GRAN_PER_THREAD, smooth_k=False, p_max="final")
-    b = sage_attention(q, k, v, accum=accum, gran=GRAN_PER_THREAD, smooth_k=False, p_max="running")
+    b = sage_attention(q, k, v, accum=accum, gran=GRAN_PER_THREAD, smooth_k=False, p_max="running",
+                       key_tile=key_tile)
     for h in range(2):                                 # the premise: key 0 is every row's max
         kq, qq = a["kv"][(0, h)], a["q"][(0, h)]
         t = (qq["q8"].astype(np.float64) @ kq["k8"].astype(np.float64).T

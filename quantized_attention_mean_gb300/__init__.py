@@ -326,6 +326,14 @@ def e4m3(x, stream=None):
     return out
 
 
+def select_path(path="auto"):
+    """Which implementation dense calls use: "auto" / "main" (the main pipeline, four launches)
+    or "short" (the one-launch short-sequence kernel for problems with at most 256 keys and
+    1024 queries; larger ones still take the main pipeline). Process-wide."""
+    _check(_lib.load().sage_debug_select_path({"auto": 0, "main": 1, "short": 2}[path]),
+           "sage_debug_select_path")
+
+
 def profile_enable(on=True):
     _check(_lib.load().sage_profile_enable(int(bool(on))), "sage_profile_enable")
 

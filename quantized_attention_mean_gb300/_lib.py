@@ -48,6 +48,7 @@ SIGNATURES = {
     "sage_debug_e4m3": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
     "sage_profile_enable": (c_int, [c_int]),
     "sage_debug_stall_attention": (c_int, [c_int]),
+    "sage_debug_select_path": (c_int, [c_int]),
     "sage_debug_trace_attention": (c_int, [c_void_p]),
     "sage_profile_read": (c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)]),
     # outs (array of sage_tensor), lses (array of float*), n, out, lse_out, B, H, N, d, dtype,

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsageattn.so")
-SOURCES = ["api.cu", "quant.cu", "attention.cu", "no_alloc.cu", "merge.cu"]
+SOURCES = ["api.cu", "quant.cu", "attention.cu", "no_alloc.cu", "merge.cu", "short.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          f"-I{ROOT}/include"]

@@ -75,7 +75,24 @@ def gpu_kw(w: Workload):
                 smooth_v=w.smooth_v)
 
 
-def run_gpu_dense(w: Workload, q, k, v, sm_scale=None, debug_scores=False):
+def short_eligible(w: Workload):
+    """Whether the one-launch short-sequence kernel can take this dense problem."""
+    return w.Nk <= 256 and w.Nq <= 1024 and w.extra.get("pv", "fp8") == "fp8"
+
+
+def run_gpu_dense(w: Workload, q, k, v, sm_scale=None, debug_scores=False, path="auto"):
+    """One sage_attn call. path: "auto" / "main" (the main pipeline) or "short" (the one-launch
+    short-sequence kernel; the problem must be short_eligible and no score dump requested)."""
+    import quantized_attention_mean_gb300 as qa
+    assert path != "short" or (short_eligible(w) and not debug_scores)
+    qa.select_path(path)
+    try:
+        return _run_gpu_dense(w, q, k, v, sm_scale, debug_scores)
+    finally:
+        qa.select_path("auto")
+
+
+def _run_gpu_dense(w, q, k, v, sm_scale, debug_scores):
     import quantized_attention_mean_gb300 as qa
     dev = torch.device("cuda:0")
     qd, kd, vd = (t.to(dev) for t in (q, k, v))

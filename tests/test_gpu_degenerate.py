@@ -6,7 +6,9 @@ the fp16 subnormals. (Scores far beyond fp32's resolution, e.g. both Q and K in 
 are outside the method: its softmax runs in fp32, so the oracle's fp64 ranking of near-equal
 maxima cannot be reproduced there.)
 Bit-exact where the codes, scales and scores are compared; the output within the usual
-tolerance, or exact where the mathematics makes it exact."""
+tolerance, or exact where the mathematics makes it exact. Every case runs on both
+implementations of a dense call (the main pipeline and the one-launch short-sequence
+kernel)."""
 
 import numpy as np
 import pytest
@@ -15,14 +17,20 @@ import torch
 from oracle.attention import sage_attention
 from quantized_attention_mean_gb300.workloads import Workload, dense_inputs, to_hnd_f32
 
-from helpers import TOL_COS, TOL_LSE, TOL_MAX_ABS, cosine, max_abs_excess, oracle_kw, out_to_hnd, run_gpu_dense
+from helpers import (TOL_COS, TOL_LSE, TOL_MAX_ABS, cosine, max_abs_excess, oracle_kw, out_to_hnd, run_gpu_dense,
+                     short_eligible)
 
 pytestmark = pytest.mark.gpu
 
 
-def _check(w, q, k, v, exact_out=False):
+PATHS = ["main", "short"]
+
+
+def _check(w, q, k, v, exact_out=False, path="main"):
     import quantized_attention_mean_gb300 as qa
-    g = run_gpu_dense(w, q, k, v, debug_scores=True)
+    if path == "short" and not short_eligible(w):
+        pytest.skip("too long for the short-sequence kernel")
+    g = run_gpu_dense(w, q, k, v, debug_scores=path == "main", path=path)
     assert g["status"] == 0
     qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
     ref = sage_attention(qn, kn, vn, **oracle_kw(w))
@@ -50,23 +58,26 @@ def _check(w, q, k, v, exact_out=False):
     return o, g, ref
 
 
-def test_all_zero_inputs():
-    w = Workload("zeros", 1, 2, 2, 200, 300, 64, gran="per_warp", return_lse=True, smooth_v=True)
+@pytest.mark.parametrize("path", PATHS)
+def test_all_zero_inputs(path):
+    w = Workload("zeros", 1, 2, 2, 200, 250, 64, gran="per_warp", return_lse=True, smooth_v=True)
     q, k, v = (torch.zeros_like(t) for t in dense_inputs(w, 0))
-    o, g, ref = _check(w, q, k, v, exact_out=True)
+    o, g, ref = _check(w, q, k, v, exact_out=True, path=path)
     assert not o.any()
     # every score 0: the LSE is ln(Nk) exactly up to the log's rounding
     np.testing.assert_allclose(g["lse"].cpu().numpy(), np.log(w.Nk), atol=1e-5)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_keys_constant_over_tokens(causal):
-    w = Workload("const_k", 2, 4, 2, 260, 260, 128, dtype="bf16", layout="NHD", is_causal=causal,
+def test_keys_constant_over_tokens(causal, path):
+    w = Workload("const_k", 2, 4, 2, 250, 250, 128, dtype="bf16", layout="NHD", is_causal=causal,
                  gran="per_thread", accum="fp32", return_lse=True)
     q, k, v = dense_inputs(w, 1)
     k = k[:, :1].expand_as(k).contiguous()          # NHD: the first token's keys everywhere
-    o, g, ref = _check(w, q, k, v)
-    assert not g["scores"].cpu().numpy()[g["scores"].cpu().numpy() != -2**31].any()
+    o, g, ref = _check(w, q, k, v, path=path)
+    if path == "main":
+        assert not g["scores"].cpu().numpy()[g["scores"].cpu().numpy() != -2**31].any()
     # uniform attention: the (causal) running mean of V, up to V's E4M3 rounding (rows that
     # average at least 32 keys)
     vn = to_hnd_f32(v, w.layout).astype(np.float64)
@@ -77,19 +88,21 @@ def test_keys_constant_over_tokens(causal):
         assert np.abs(o[0, h, 31:] - mean[31:]).max() < 0.05
 
 
-def test_values_constant_over_tokens():
-    w = Workload("const_v", 1, 2, 1, 150, 333, 64, gran="per_block", accum="fp16+fp32", smooth_v=True,
+@pytest.mark.parametrize("path", PATHS)
+def test_values_constant_over_tokens(path):
+    w = Workload("const_v", 1, 2, 1, 150, 233, 64, gran="per_block", accum="fp16+fp32", smooth_v=True,
                  return_lse=True)
     q, k, v = dense_inputs(w, 2)
     v = v[:, :, :1].expand_as(v).contiguous()       # HND: the first token's values everywhere
-    o, g, ref = _check(w, q, k, v)
+    o, g, ref = _check(w, q, k, v, path=path)
     # V' = 0 and s_v = 0: the output is v-mean, i.e. the constant row, in every query row
     vrow = v[0, 0, 0].float().numpy()
     assert np.array_equal(o[0, 0], np.broadcast_to(vrow, o[0, 0].shape))
     assert np.array_equal(o[0, 1], np.broadcast_to(vrow, o[0, 1].shape))
 
 
-def test_inputs_at_the_fp16_extremes():
+@pytest.mark.parametrize("path", PATHS)
+def test_inputs_at_the_fp16_extremes(path):
     # Q near the fp16 maximum, K down among fp16 subnormals (their products, and so the
     # softmax, stay ordinary): the scales and the fixed-point K mean at both ends of the range
     w = Workload("extremes", 1, 2, 2, 256, 256, 64, gran="per_thread", accum="fp32", return_lse=True,
@@ -98,4 +111,4 @@ def test_inputs_at_the_fp16_extremes():
     q = (q.float() * 1.5e4).clamp(-6.5e4, 6.5e4).half()
     k = (k.float() * 4e-5).half()
     assert (k.abs() < 6.1e-5).float().mean() > 0.5  # mostly subnormal
-    _check(w, q, k, v)
+    _check(w, q, k, v, path=path)

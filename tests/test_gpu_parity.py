@@ -1,4 +1,7 @@
-"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI, for both
+implementations of a dense call: the main pipeline (statistics, quantisation and the tcgen05
+attention kernel) and the one-launch short-sequence kernel (cases with at most 512 keys and
+1024 queries).
 
 Bit-exact: INT8 Q/K codes and their scales, the smoothing means, FP8 V codes and scales,
 and the integer scores S = Q8·K8^T as the attention kernel reads them from tensor memory.
@@ -20,7 +23,7 @@ from oracle.fp8 import e4m3_encode
 from quantized_attention_mean_gb300.workloads import WORKLOADS, Workload, dense_inputs, to_hnd_f32
 
 from helpers import (TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, assert_online_parity, cosine,
-                     max_abs_excess, oracle_kw, out_to_hnd, run_gpu_dense)
+                     max_abs_excess, oracle_kw, out_to_hnd, run_gpu_dense, short_eligible)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,19 +52,25 @@ CASES = [
 ]
 
 
-def _run(w, seed=0):
+PATHS = ["main", "short"]
+
+
+def _run(w, seed=0, path="main"):
+    if path == "short" and not short_eligible(w):
+        pytest.skip("too long for the short-sequence kernel")
     q, k, v = dense_inputs(w, seed)
-    g = run_gpu_dense(w, q, k, v, debug_scores=True)
+    g = run_gpu_dense(w, q, k, v, debug_scores=path == "main", path=path)
     assert g["status"] == 0
     qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
     ref = sage_attention(qn, kn, vn, **oracle_kw(w))
     return q, k, v, qn, kn, vn, g, ref
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_quantisation_bit_exact(w):
+def test_quantisation_bit_exact(w, path):
     import quantized_attention_mean_gb300 as qa
-    _, _, _, qn, kn, vn, g, ref = _run(w)
+    _, _, _, qn, kn, vn, g, ref = _run(w, path=path)
     ex = {k: t.cpu().numpy() for k, t in qa.export_quant(g["ws"], w.B, w.Hq, w.Hkv, w.Nq, w.Nk,
                                                           w.d, w.gran).items()}
     for b in range(w.B):
@@ -95,9 +104,10 @@ def test_scores_bit_exact(w):
                 np.testing.assert_array_equal(s[b, h], exact)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_output_within_tolerance(w):
-    _, _, _, qn, kn, vn, g, ref = _run(w)
+def test_output_within_tolerance(w, path):
+    _, _, _, qn, kn, vn, g, ref = _run(w, path=path)
     o = out_to_hnd(g["out"], w.layout)
     o_ref = ref["o"]
     assert np.isfinite(o).all()
@@ -113,13 +123,16 @@ def test_output_within_tolerance(w):
         assert np.abs(lse - ref["lse"]).max() <= TOL_LSE
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_output_matches_online_form(w):
-    # the kernel's softmax is the online form (P~ against the running maximum of the 128-key
+def test_output_matches_online_form(w, path):
+    # both kernels' softmax is the online form (P~ against the running maximum of the 128-key
     # tiles seen so far); against the oracle's online form almost every element agrees to
     # 1e-3 and the cosine to 1e-5 (what is left: ex2.approx vs exp and fp32 sums)
+    if path == "short" and not short_eligible(w):
+        pytest.skip("too long for the short-sequence kernel")
     q, k, v = dense_inputs(w, 0)
-    g = run_gpu_dense(w, q, k, v)
+    g = run_gpu_dense(w, q, k, v, path=path)
     assert g["status"] == 0
     qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
     ref = sage_attention(qn, kn, vn, p_max="running", **oracle_kw(w))

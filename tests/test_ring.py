@@ -116,3 +116,27 @@ def test_ring_bookkeeping():
             assert sorted(ring_chunk(rank, world, s) for s in range(world)) == list(range(world))
     assert chunk_mode(2, 1, True) == "full" and chunk_mode(2, 2, True) == "causal"
     assert chunk_mode(2, 3, True) == "none" and chunk_mode(2, 3, False) == "full"
+
+
+@pytest.mark.gpu
+def test_ring_default_path_on_one_gpu():
+    # a one-rank group runs the default compute (sage_attn with return_lse, merge_partials)
+    # with no exchange: the merge of the single partial is the partial itself
+    import torch.distributed as dist
+    import quantized_attention_mean_gb300 as qa
+    from quantized_attention_mean_gb300.ring import ring_attention
+    dev = torch.device("cuda:0")
+    q, k, v = (t.half().to(dev) for t in _inputs(1, 300, seed=3))
+    store = dist.HashStore()
+    group_init = not dist.is_initialized()
+    if group_init:
+        dist.init_process_group("gloo", store=store, rank=0, world_size=1)
+    try:
+        o, l = ring_attention(q, k, v, is_causal=True, smooth_v=True)
+        ref_o, ref_l = qa.sage_attn(q, k, v, is_causal=True, return_lse=True, smooth_v=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o)
+        assert torch.allclose(l, ref_l, rtol=0, atol=1e-6)
+    finally:
+        if group_init:
+            dist.destroy_process_group()

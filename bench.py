@@ -39,7 +39,12 @@ L2_BYTES = 129 * 2**20
 # full launch by the units processed where the full size is too large to capture), with the
 # SHA-256 of the attention kernel's source at capture time: the figure is reported only while
 # the source is unchanged.
-ATTN_DRAM_BYTES = {}
+ATTN_DRAM_BYTES = {
+    "dit17776_h24": (996899328, "b5bf71964cc0735b",
+                     "captured: 944169984 read + 52729344 written"),
+    "dit17776": (3987597312, "b5bf71964cc0735b",
+                 "the B=1 H=24 capture x 4 (B=2 H=48: 4x the heads, same per-head work)"),
+}
 
 
 def attention_source_digest():
@@ -52,8 +57,8 @@ def attention_source_digest():
 def measured_traffic(wname):
     entry = ATTN_DRAM_BYTES.get(wname)
     if entry is None or entry[1] != attention_source_digest():
-        return None
-    return entry[0]
+        return None, "no ncu capture of the current kernel source for this workload"
+    return entry[0], "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch; " + entry[2]
 
 
 def parse():
@@ -188,20 +193,35 @@ def parse_clock_samples(text):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+# Arm (implementer, part) codes as /proc/cpuinfo prints them, for hosts whose kernel gives no
+# model name
+ARM_PARTS = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+             ("0x41", "0xd0c"): "Arm Neoverse-N1", ("0x41", "0xd49"): "Arm Neoverse-N2"}
+
+
 def host_cpu():
     """(logical cores, CPU model string) of this host."""
-    model = "unknown"
+    import platform
+    model = None
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
-                key = ln.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware") and ":" in ln:
-                    model = ln.split(":", 1)[1].strip()
-                    break
+                if ":" not in ln:
+                    continue
+                key, val = (x.strip() for x in ln.split(":", 1))
+                fields.setdefault(key.lower(), val)
     except OSError:
         pass
-    if model == "unknown":
-        import platform
+    for key in ("model name", "cpu model", "hardware"):
+        if fields.get(key):
+            model = fields[key]
+            break
+    if model is None and "cpu implementer" in fields:
+        imp, part = fields["cpu implementer"], fields.get("cpu part", "?")
+        model = ARM_PARTS.get((imp.lower(), part.lower()),
+                              f"{platform.machine()} (implementer {imp}, part {part})")
+    if model is None:
         model = platform.processor() or platform.machine()
     return os.cpu_count() or 1, model
 
@@ -466,8 +486,9 @@ def run_ours(args, w):
              + n_kv * (4 if pv16 else 3))                # V: 2 read + 1 (fp16 variant: 2) written
     pre_ms = (stage_ms[0] + stage_ms[1]) / per
     pre_gbs = alg_bytes / (pre_ms / 1e3) / 1e9
+    traffic, traffic_src = measured_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": kpeak, "unit": "TFLOP/s",
-                "frac": achieved / kpeak, "traffic": measured_traffic(w.name),
+                "frac": achieved / kpeak, "traffic": traffic, "traffic_source": traffic_src,
                 "kernel": f"attn_kernel<{64 if w.d <= 64 else 128}, {1 if pv16 else 0}> "
                           "(fused QK^T/softmax/PV)",
                 "peak_source": (f"{pk['src']}: dense fp16 = bf16 burst {pk['bf16']} TFLOP/s" if pv16 else

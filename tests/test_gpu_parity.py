@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path against the CPU oracle, through the C ABI, for both
 implementations of a dense call: the main pipeline (statistics, quantisation and the tcgen05
-attention kernel) and the one-launch short-sequence kernel (cases with at most 512 keys and
+attention kernel) and the one-launch short-sequence kernel (cases with at most 256 keys and
 1024 queries).
 
 Bit-exact: INT8 Q/K codes and their scales, the smoothing means, FP8 V codes and scales,

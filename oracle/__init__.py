@@ -32,8 +32,15 @@ Parity status per function (see the pins in ``tests/test_oracle_*.py``):
                                           arithmetic, σ_P = 448: a two-key case worked by hand
                                           from the E4M3 table, identical-key and single-key
                                           closed forms in every mode)
+  fp4.e2m1_encode / e2m1_decode          pinned (value table from the field layout, brute-force
+                                          nearest value with ties to the even mantissa)
+  fp4.microscale_blocks / fp4_*_quant    pinned (block-step properties, a hand-worked block,
+                                          reconstruction bound, lossless inputs round-trip)
+  attention FP4 variant (pv="fp4")       pinned (single-key and two-key closed forms on inputs
+                                          FP4 represents exactly; bypass == fp64 attention;
+                                          one tile: online == final form)
   merge.merge_partials                   pinned (chunked fp64 attention merges to the unchunked
                                           result; empty parts; single part; order invariance)
 """
 
-from . import fp8, quant, attention, merge  # noqa: F401
+from . import fp4, fp8, quant, attention, merge  # noqa: F401

@@ -42,10 +42,19 @@ FP16 P·V variant (pv="fp16"; the guide's §5.3 / §5.4 INT8-QK + FP16-PV kernel
 fallback with FP8 turned off): step 3 keeps V' as fp16 (RNE) instead of E4M3 with a scale,
 step 7 rounds P to fp16 with σ_P = 1, and step 9 has no V scale. Steps 4-6, 8 and 10 are
 unchanged.
+
+FP4 microscaled variant (pv="fp4"; the guide's §5.5 SageAttention3, "FP4 microscaling", read
+as in oracle/fp4.py): step 3 quantises Q and K' to two-level FP4 (first-level scales g_q, g_k
+per token group, E4M3 block scales per 16 channels) and V' likewise (g_v per channel, blocks of
+16 tokens); each code enters the products as its carrier c · s_b ≈ 6 u. Step 4 multiplies the
+carriers (S ≈ 36 · q·k / (g_q g_k)), so step 5 scales by g_q g_k / 36; step 7 quantises
+y = fl32(448 p) in blocks of 16 keys (P's carrier ≈ 6 · 448 p: σ_P = 2688); step 9 scales by
+g_v / 6. Steps 6, 8 and 10 are unchanged.
 """
 
 import numpy as np
 
+from .fp4 import fp4_channel_quant, fp4_group_quant, fp4_p
 from .fp8 import e4m3_decode, e4m3_encode
 from .quant import (GRAN_PER_BLOCK, GRAN_PER_THREAD, GRAN_PER_WARP, K_GROUP, Q_GROUP,
                     fixed_point_mean, fp8_channel_quant, int8_group_quant, smooth)
@@ -97,7 +106,8 @@ def to_bf16(x):
 
 # --------------------------------------------------------------------------- stages 1-3
 def quantize_kv_head(k, v, gran, smooth_k, smooth_v, pv="fp8"):
-    """Stages 1-3 for one KV head: k, v float32 [Nk, d]. pv="fp16" keeps V' in fp16."""
+    """Stages 1-3 for one KV head: k, v float32 [Nk, d]. pv="fp16" keeps V' in fp16;
+    pv="fp4" quantises K' and V' to two-level FP4 (oracle/fp4.py)."""
     k = np.asarray(k, np.float32)
     v = np.asarray(v, np.float32)
     d = k.shape[1]
@@ -105,18 +115,29 @@ def quantize_kv_head(k, v, gran, smooth_k, smooth_v, pv="fp8"):
     vbar = fixed_point_mean(v) if smooth_v else np.zeros(d, np.float32)
     ks = smooth(k, kbar)
     vs = smooth(v, vbar)
+    if pv == "fp4":
+        kq = fp4_group_quant(ks, K_GROUP[gran])
+        vq = fp4_channel_quant(vs)
+        return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k4=kq["carrier"],
+                    sk=kq["scales"], k_codes=kq["codes"], k_block_scales=kq["block_scales"],
+                    v4=vq["carrier"], sv=vq["scales"], v_codes=vq["codes"],
+                    v_block_scales=vq["block_scales"], pv="fp4")
     k8, sk = int8_group_quant(ks, K_GROUP[gran])
     if pv == "fp16":
         return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk,
                     v16=to_fp16(vs), pv="fp16")
     if pv != "fp8":
-        raise ValueError("pv must be 'fp8' or 'fp16'")
+        raise ValueError("pv must be 'fp8', 'fp16' or 'fp4'")
     v8, sv = fp8_channel_quant(vs)
     return dict(kbar=kbar, vbar=vbar, k_smoothed=ks, v_smoothed=vs, k8=k8, sk=sk, v8=v8, sv=sv,
                 pv="fp8")
 
 
-def quantize_q_head(q, gran):
+def quantize_q_head(q, gran, pv="fp8"):
+    if pv == "fp4":
+        qq = fp4_group_quant(np.asarray(q, np.float32), Q_GROUP[gran])
+        return dict(q4=qq["carrier"], sq=qq["scales"], q_codes=qq["codes"],
+                    q_block_scales=qq["block_scales"])
     q8, sq = int8_group_quant(np.asarray(q, np.float32), Q_GROUP[gran])
     return dict(q8=q8, sq=sq)
 
@@ -147,12 +168,15 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
         raise ValueError("key_tile must be positive")
     q = np.asarray(q, np.float32)
     nq, d = q.shape
-    nk = kvq["k8"].shape[0]
+    nk = kvq["k_smoothed"].shape[0]
     rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
     pv16 = kvq.get("pv") == "fp16"
+    pv4 = kvq.get("pv") == "fp4"
     sig = sigma_p(accum)       # raises for pure fp16 accumulation or an unknown mode
     if pv16:
         sig = 1.0              # fp16 P needs no scaling into its format's range
+    if pv4:
+        sig = 448.0 * 6.0      # P's carrier is ~6 · 448 p
     if bypass_quant is True:
         qv = q.astype(np.float64)
         sq_row = np.ones(nq)
@@ -167,13 +191,23 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
         sk_key = np.ones(nk)
     else:
         if qq is None:
-            qq = quantize_q_head(q, gran)
-        qv = qq["q8"].astype(np.float64)
-        sq_row = qq["sq"].astype(np.float64)[np.arange(nq) // Q_GROUP[gran]]
-        kv = kvq["k8"].astype(np.float64)
-        sk_key = kvq["sk"].astype(np.float64)[np.arange(nk) // K_GROUP[gran]]
+            qq = quantize_q_head(q, gran, pv="fp4" if pv4 else "fp8")
+        if pv4:
+            # carriers ≈ 6 x / g: the score scale carries g_q g_k / 36
+            qv = qq["q4"]
+            sq_row = qq["sq"].astype(np.float64)[np.arange(nq) // Q_GROUP[gran]] / 6.0
+            kv = kvq["k4"]
+            sk_key = kvq["sk"].astype(np.float64)[np.arange(nk) // K_GROUP[gran]] / 6.0
+        else:
+            qv = qq["q8"].astype(np.float64)
+            sq_row = qq["sq"].astype(np.float64)[np.arange(nq) // Q_GROUP[gran]]
+            kv = kvq["k8"].astype(np.float64)
+            sk_key = kvq["sk"].astype(np.float64)[np.arange(nk) // K_GROUP[gran]]
     if bypass_quant is not True:
-        if pv16:
+        if pv4:
+            vd = kvq["v4"]
+            sv = kvq["sv"].astype(np.float64) / 6.0
+        elif pv16:
             vd = kvq["v16"].astype(np.float64)
             sv = np.ones(d)
         else:
@@ -197,6 +231,8 @@ def attend_head(q, kvq, *, gran, sm_scale, is_causal, accum, rows=None, qq=None,
                 return p * sig
             if pv16:
                 return to_fp16(p)
+            if pv4:
+                return fp4_p(p, 448.0)
             return e4m3_decode(e4m3_encode(p * sig))
 
         if p_max == "final":
@@ -261,7 +297,7 @@ def sage_attention(q, k, v, *, is_causal=False, sm_scale=None, gran=GRAN_PER_WAR
         if key not in kvcache:
             kvcache[key] = quantize_kv_head(k[b, h // group], v[b, h // group], gran,
                                             smooth_k, smooth_v, pv=pv)
-        qcache[(b, h)] = quantize_q_head(q[b, h], gran)
+        qcache[(b, h)] = quantize_q_head(q[b, h], gran, pv="fp4" if pv == "fp4" else "fp8")
         res = attend_head(q[b, h], kvcache[key], gran=gran, sm_scale=sm_scale,
                           is_causal=is_causal, accum=accum, rows=rows, qq=qcache[(b, h)],
                           bypass_quant=bypass_quant, p_max=p_max, key_tile=key_tile)

@@ -62,4 +62,4 @@ def test_fp16_pv_is_closer_to_exact_than_fp8():
 def test_rejects_unknown_pv():
     q, k, v = _rand(5, 4, 4, 8)
     with pytest.raises(ValueError):
-        quantize_kv_head(k, v, GRAN_PER_WARP, True, False, pv="fp4")
+        quantize_kv_head(k, v, GRAN_PER_WARP, True, False, pv="int4")

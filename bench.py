@@ -254,8 +254,9 @@ def oracle_rows(path, r0, r1, wname):
     q, k, v = z["q"], z["k"], z["v"]
     g = GRAN[w.gran]
     t0 = time.perf_counter()
-    kvq = quantize_kv_head(k, v, g, w.smooth_k, w.smooth_v, pv=w.extra.get("pv", "fp8"))
-    qq = quantize_q_head(q, g)
+    pv = w.extra.get("pv", "fp8")
+    kvq = quantize_kv_head(k, v, g, w.smooth_k, w.smooth_v, pv=pv)
+    qq = quantize_q_head(q, g, pv="fp4" if pv == "fp4" else "fp8")
     attend_head(q, kvq, gran=g, sm_scale=default_sm_scale(w.d), is_causal=w.is_causal,
                 accum=ACC[w.accum], rows=np.arange(r0, r1), qq=qq)
     t1 = time.perf_counter()
@@ -379,7 +380,8 @@ def run_ours(args, w):
               pv_accum_dtype=w.accum, smooth_k=w.smooth_k, smooth_v=w.smooth_v)
     stream = torch.cuda.current_stream()
     # the FP16 P·V variant has its own entry point
-    dense_call = qa.sage_attn_qk_int8_pv_fp16 if w.extra.get("pv") == "fp16" else qa.sage_attn
+    dense_call = {"fp16": qa.sage_attn_qk_int8_pv_fp16, "fp4": qa.sage_attn_fp4}.get(
+        w.extra.get("pv"), qa.sage_attn)
 
     def step(i):
         q, k, v, out, lse, ws, cu = sets[i % nsets]
@@ -467,7 +469,8 @@ def run_ours(args, w):
     per = max(calls, 1)
     attn_ms = stage_ms[2] / per
     achieved = ops / (attn_ms / 1e3) / 1e12
-    pv16 = w.extra.get("pv") == "fp16"
+    pvfmt = w.extra.get("pv", "fp8")
+    pv16 = pvfmt in ("fp16", "fp4")   # both products on fp16 operands (kind::f16)
     fp8_peak = 2.0 * pk["bf16"]
     kpeak = pk["bf16"] if pv16 else fp8_peak
     kpeak_sust = pk["bf16_sust"] if pv16 else 2.0 * pk["bf16_sust"]
@@ -483,13 +486,13 @@ def run_ours(args, w):
     alg_bytes = 3 * (n_q + 2 * n_kv)
     moved = (2 * n_kv * (2 if w.smooth_k else 1)      # statistics: V (and K) read
              + 4 * n_q + 4 * n_kv                        # Q, K: 2 read + 2 written
-             + n_kv * (4 if pv16 else 3))                # V: 2 read + 1 (fp16 variant: 2) written
+             + n_kv * (4 if pv16 else 3))                # V: 2 read + 1 (fp16 carriers: 2) written
     pre_ms = (stage_ms[0] + stage_ms[1]) / per
     pre_gbs = alg_bytes / (pre_ms / 1e3) / 1e9
     traffic, traffic_src = measured_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": kpeak, "unit": "TFLOP/s",
                 "frac": achieved / kpeak, "traffic": traffic, "traffic_source": traffic_src,
-                "kernel": f"attn_kernel<{64 if w.d <= 64 else 128}, {1 if pv16 else 0}> "
+                "kernel": f"attn_kernel<{64 if w.d <= 64 else 128}, {dict(fp8=0, fp16=1, fp4=2)[pvfmt]}> "
                           "(fused QK^T/softmax/PV)",
                 "peak_source": (f"{pk['src']}: dense fp16 = bf16 burst {pk['bf16']} TFLOP/s" if pv16 else
                                 f"{pk['src']}: dense FP8 = 2 x bf16 burst {pk['bf16']} TFLOP/s"),
@@ -591,7 +594,10 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
             "windows": {"count": n_windows, "statistic": "median", "ms": [round(x, 4) for x in window_ms]},
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8 QK (exact, fp16 carrier) + " + ("fp16" if w.extra.get("pv") == "fp16" else "e4m3") + " PV, fp32 softmax",
+            "scaling": "weak", "vs_baseline": None, "dtype": ("fp4 e2m1 x e4m3 microscaled QK and PV (exact fp16 carriers), fp32 softmax"
+                      if pvfmt == "fp4" else
+                      "int8 QK (exact, fp16 carrier) + " + ("fp16" if pvfmt == "fp16" else "e4m3")
+                      + " PV, fp32 softmax"),
             "data": "synthetic",
             "config": {"workload": describe(w), "parallelism": f"replicas x{ws_n} (independent heads/batches)",
                        "l2": f"inputs rotate over {nsets} resident sets ({nsets * (per_set + wsb) / 2**20:.0f} MiB > L2 129 MiB)",

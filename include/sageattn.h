@@ -122,6 +122,26 @@ int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const 
                               int qk_quant_gran, int pv_accum_dtype, int smooth_k, int smooth_v,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* FP4 microscaled variant (pwwt.cn "SageAttention deployment pitfalls guide" §5.5: the
+ * SageAttention3 kernel for Blackwell, "FP4 microscaling"; the guide names only its API,
+ * sageattn3_blackwell(q, k, v, is_causal)): as sage_attn, with the same arguments, workspace
+ * size and errors, except for the quantisation:
+ *   Q and K' = K - k̄: each token group (qk_quant_gran) is mapped onto [-448, 448] by its
+ *   scale g = absmax / 448; every 16 channels of a row share an E4M3 block scale s (the
+ *   block's largest mapped magnitude, rounded) and each element is the E2M1 code of
+ *   fl32(u · fl32(6 / s)), RNE, saturating at ±6.
+ *   V' = V - v̄: each channel is mapped by absmax_c / 448 and blocked over 16 tokens.
+ *   P: 448 · 2^(t - m), blocked over 16 keys.
+ * Every E2M1 code times its E4M3 block scale is exact in fp16, so both products run on
+ * fp16 tensor cores (kind::f16) and give what a block-scaled FP4 product gives. P·V
+ * accumulates in fp32; pv_accum_dtype as for sage_attn. Dense problems only. */
+int sage_attn_fp4(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                  const sage_tensor* out, float* lse, int batch, int heads_q, int heads_kv,
+                  int seqlen_q, int seqlen_k, int head_dim, int dtype, int tensor_layout,
+                  int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+                  int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
 /* Capacity of the scratch array built into the library for sage_attn_no_alloc. */
 #define SAGE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -279,6 +299,19 @@ int sage_debug_trace_attention(long long* clocks);
 /* Converts n floats (device) to FP8 E4M3 (device bytes) with the round-to-nearest-even,
  * saturating conversion the kernels use for V and P. */
 int sage_debug_e4m3(const float* x, uint8_t* out, int64_t n, void* stream);
+
+/* Converts n floats (device) to FP4 E2M1 codes (device bytes, low 4 bits) with the
+ * round-to-nearest-even conversion saturating at ±6 that the FP4 variant uses. */
+int sage_debug_e2m1(const float* x, uint8_t* out, int64_t n, void* stream);
+
+/* Copies the fp16 operands the attention kernel consumed after a dense call of the FP16 P·V
+ * or FP4 variant into canonical layouts (device buffers of fp16 bit patterns):
+ *   q16 [B, Hq, Nq, d] and k16 [B, Hkv, Nk, d] (the FP4 carriers; INT8 codes as fp16 after
+ *   the other dense calls), v16 [B, Hkv, Nk, d] (V' in fp16, or the FP4 carriers of V).
+ * Any output pointer may be NULL to skip it. */
+int sage_debug_export_fp16(const void* workspace, int batch, int heads_q, int heads_kv,
+                           int seqlen_q, int seqlen_k, int head_dim, int qk_quant_gran,
+                           uint16_t* q16, uint16_t* k16, uint16_t* v16, void* stream);
 
 #ifdef __cplusplus
 }

@@ -115,7 +115,8 @@ def _dims(q, k, layout):
 
 def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, return_lse=False,
               qk_quant_gran="per_warp", pv_accum_dtype="fp32", smooth_k=True, smooth_v=False,
-              out=None, lse=None, workspace=None, stream=None, _debug_scores=None, _pv16=False):
+              out=None, lse=None, workspace=None, stream=None, _debug_scores=None, _pv16=False,
+              _fp4=False):
     """Quantized attention forward. q: [B, Hq, Nq, d] (HND) or [B, Nq, Hq, d] (NHD);
     k, v: [B, Hkv, Nk, d] / [B, Nk, Hkv, d]; fp16 or bf16 on one CUDA device.
     Returns out (same shape/layout/dtype as q), plus lse [B, Hq, Nq] fp32 if return_lse."""
@@ -137,7 +138,9 @@ def sage_attn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, retu
             int(bool(smooth_k)), int(bool(smooth_v)), ctypes.c_void_p(workspace.data_ptr()),
             workspace.numel()]
     with torch.cuda.device(q.device):
-        if _pv16:
+        if _fp4:
+            st = lib.sage_attn_fp4(*args, _stream_ptr(stream))
+        elif _pv16:
             st = lib.sage_attn_qk_int8_pv_fp16(*args, _stream_ptr(stream))
         elif _debug_scores is None:
             st = lib.sage_attn(*args, _stream_ptr(stream))
@@ -159,6 +162,18 @@ def sage_attn_qk_int8_pv_fp16(q, k, v, tensor_layout="HND", is_causal=False, sm_
                      return_lse=return_lse, qk_quant_gran=qk_quant_gran,
                      pv_accum_dtype=pv_accum_dtype, smooth_k=smooth_k, smooth_v=smooth_v, out=out,
                      lse=lse, workspace=workspace, stream=stream, _pv16=True)
+
+
+def sage_attn_fp4(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None, return_lse=False,
+                  qk_quant_gran="per_warp", pv_accum_dtype="fp32", smooth_k=True, smooth_v=False,
+                  out=None, lse=None, workspace=None, stream=None):
+    """The FP4 microscaled variant (E2M1 codes with E4M3 scales per 16 elements for Q, K, P
+    and V), standing for the pages' ``sageattn3_blackwell``. Arguments and results as
+    ``sage_attn``."""
+    return sage_attn(q, k, v, tensor_layout=tensor_layout, is_causal=is_causal, sm_scale=sm_scale,
+                     return_lse=return_lse, qk_quant_gran=qk_quant_gran,
+                     pv_accum_dtype=pv_accum_dtype, smooth_k=smooth_k, smooth_v=smooth_v, out=out,
+                     lse=lse, workspace=workspace, stream=stream, _fp4=True)
 
 
 def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
@@ -316,6 +331,33 @@ def export_quant(workspace, B, Hq, Hkv, Nq, Nk, d, qk_quant_gran, stream=None):
     return res
 
 
+def export_fp16(workspace, B, Hq, Hkv, Nq, Nk, d, qk_quant_gran, stream=None):
+    """Copies the fp16 operands (Q and K codes or FP4 carriers, V' in fp16 or its FP4
+    carriers) a previous dense call of the FP16 P·V or FP4 variant left in `workspace`, as
+    float16 tensors [B, H, N, d]."""
+    lib = _lib.load()
+    g = GRAN[qk_quant_gran]
+    dev = workspace.device
+    res = dict(q16=torch.empty((B, Hq, Nq, d), dtype=torch.float16, device=dev),
+               k16=torch.empty((B, Hkv, Nk, d), dtype=torch.float16, device=dev),
+               v16=torch.empty((B, Hkv, Nk, d), dtype=torch.float16, device=dev))
+    st = lib.sage_debug_export_fp16(ctypes.c_void_p(workspace.data_ptr()), B, Hq, Hkv, Nq, Nk, d, g,
+                                    *[ctypes.c_void_p(res[n].data_ptr()) for n in ("q16", "k16", "v16")],
+                                    _stream_ptr(stream))
+    _check(st, "sage_debug_export_fp16")
+    return res
+
+
+def e2m1(x, stream=None):
+    """FP4 E2M1 conversion with the kernels' rounding (test hook): float32 CUDA -> uint8 codes."""
+    lib = _lib.load()
+    x = x.contiguous()
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib.sage_debug_e2m1(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                               x.numel(), _stream_ptr(stream)), "sage_debug_e2m1")
+    return out
+
+
 def e4m3(x, stream=None):
     """FP8 E4M3 conversion with the kernels' rounding (test hook): float32 CUDA -> uint8."""
     lib = _lib.load()
@@ -350,6 +392,7 @@ def default_sm_scale(head_dim):
     return 1.0 / math.sqrt(head_dim)
 
 
-__all__ = ["sage_attn", "sage_attn_varlen", "SageError", "workspace_bytes",
-           "varlen_workspace_bytes", "alloc_workspace", "read_device_status", "export_quant", "e4m3",
+__all__ = ["sage_attn", "sage_attn_varlen", "sage_attn_fp4", "SageError", "workspace_bytes",
+           "varlen_workspace_bytes", "alloc_workspace", "read_device_status", "export_quant",
+           "export_fp16", "e4m3", "e2m1",
            "profile_enable", "profile_read"]

@@ -30,6 +30,8 @@ SIGNATURES = {
                   + [c_void_p, c_size_t, c_void_p]),
     "sage_attn_qk_int8_pv_fp16": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float]
                                   + [c_int] * 5 + [c_void_p, c_size_t, c_void_p]),
+    "sage_attn_fp4": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float]
+                      + [c_int] * 5 + [c_void_p, c_size_t, c_void_p]),
     "sage_attn_no_alloc": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float] + [c_int] * 5
                            + [c_void_p]),
     "sage_attn_varlen_workspace_size": (c_size_t, [c_int] * 7),
@@ -46,6 +48,8 @@ SIGNATURES = {
     "sage_attn_debug_scores": (c_int, [_T, _T, _T, _T, c_void_p] + [c_int] * 9 + [c_float]
                                + [c_int] * 5 + [c_void_p, c_size_t, c_void_p, c_void_p]),
     "sage_debug_e4m3": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
+    "sage_debug_e2m1": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
+    "sage_debug_export_fp16": (c_int, [c_void_p] + [c_int] * 7 + [c_void_p] * 3 + [c_void_p]),
     "sage_profile_enable": (c_int, [c_int]),
     "sage_debug_stall_attention": (c_int, [c_int]),
     "sage_debug_select_path": (c_int, [c_int]),

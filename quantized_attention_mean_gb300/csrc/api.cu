@@ -281,7 +281,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                const sage_tensor* out, float* lse, int batch, int hq, int hkv, int nq, int nk,
                int d, int dtype, int layout, int is_causal, float sm_scale, int return_lse,
                int gran, int acc, int smooth_k, int smooth_v, void* ws, size_t ws_bytes,
-               int32_t* dbg_scores, void* stream, int pv16 = 0) {
+               int32_t* dbg_scores, void* stream, int pv = 0) {
   if (!q || !k || !v || !out) return SAGE_ERR_INVALID_ARG;
   const Common c{hq, hkv, d, dtype, is_causal, return_lse, gran, acc, smooth_k, smooth_v, sm_scale};
   int st = check_common(c, lse);
@@ -308,7 +308,8 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   std::memset(&p, 0, sizeof(p));
   fill_common(p, c);
   p.batch = batch; p.nq = nq; p.nk = nk; p.varlen = 0; p.vec16 = vec16 ? 1 : 0;
-  p.pv16 = pv16;
+  p.pv16 = pv != 0;  // 1: FP16 P·V variant, 2: FP4 microscaled variant (both on fp16 operands)
+  p.fp4 = pv == 2;
   // element strides (b, h, n) from the layout's dimension order
   auto bhn = [layout](const sage_tensor* t, int64_t& sb, int64_t& sh, int64_t& sn) {
     sb = t->stride[0];
@@ -330,7 +331,7 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   // variant has no short form). It is not chosen by default: measured, the main pipeline's
   // four launches replayed from a CUDA graph are faster (256^2 at head_dim 64: 22.5 us per
   // call against 36.7; direct calls 39.3 against 36.9).
-  const bool short_ok = !pv16 && !dbg_scores && !g_trace && !g_stall && nk <= kShortMaxKeys &&
+  const bool short_ok = pv == 0 && !dbg_scores && !g_trace && !g_stall && nk <= kShortMaxKeys &&
                         nq <= kShortMaxQueries;
   if (short_ok && g_path == 2) return run_short(p, L, static_cast<cudaStream_t>(stream));
   return run_pipeline(p, L, nq, nk, static_cast<cudaStream_t>(stream));
@@ -375,6 +376,18 @@ int sage_attn_qk_int8_pv_fp16(const sage_tensor* q, const sage_tensor* k, const 
                     dtype, tensor_layout, is_causal, sm_scale, return_lse, qk_quant_gran,
                     pv_accum_dtype, smooth_k, smooth_v, workspace, workspace_bytes, nullptr,
                     stream, 1);
+}
+
+int sage_attn_fp4(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                  const sage_tensor* out, float* lse, int batch, int heads_q, int heads_kv,
+                  int seqlen_q, int seqlen_k, int head_dim, int dtype, int tensor_layout,
+                  int is_causal, float sm_scale, int return_lse, int qk_quant_gran,
+                  int pv_accum_dtype, int smooth_k, int smooth_v, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  return dense_impl(q, k, v, out, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, head_dim,
+                    dtype, tensor_layout, is_causal, sm_scale, return_lse, qk_quant_gran,
+                    pv_accum_dtype, smooth_k, smooth_v, workspace, workspace_bytes, nullptr,
+                    stream, 2);
 }
 
 int sage_attn_debug_scores(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
@@ -584,6 +597,33 @@ int sage_debug_select_path(int path) {
 int sage_debug_stall_attention(int on) {
   g_stall = on ? 1 : 0;
   return SAGE_OK;
+}
+
+int sage_debug_e2m1(const float* x, uint8_t* out, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !out))) return SAGE_ERR_INVALID_ARG;
+  if (n == 0) return SAGE_OK;
+  return launch_e2m1(x, out, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAGE_OK
+                                                                                   : SAGE_ERR_CUDA;
+}
+
+int sage_debug_export_fp16(const void* workspace, int batch, int heads_q, int heads_kv,
+                           int seqlen_q, int seqlen_k, int head_dim, int qk_quant_gran,
+                           uint16_t* q16, uint16_t* k16, uint16_t* v16, void* stream) {
+  Layout L;
+  if (!workspace ||
+      !make_layout(false, batch, heads_q, heads_kv, seqlen_q, seqlen_k, head_dim, qk_quant_gran, &L))
+    return SAGE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* w = static_cast<const char*>(workspace);
+  const int pq = static_cast<int>(L.planes_q), pk = static_cast<int>(L.planes_kv);
+  bool ok = true;
+  if (q16) ok &= launch_export_fp16(reinterpret_cast<const __half*>(w + L.off_qc), L.q_rows, L.dp,
+                                    head_dim, pq, seqlen_q, q16, st) == cudaSuccess;
+  if (k16) ok &= launch_export_fp16(reinterpret_cast<const __half*>(w + L.off_kc), L.k_rows, L.dp,
+                                    head_dim, pk, seqlen_k, k16, st) == cudaSuccess;
+  if (v16) ok &= launch_export_vt16(reinterpret_cast<const __half*>(w + L.off_vt), L.vt_pitch,
+                                    L.dp, head_dim, pk, seqlen_k, v16, st) == cudaSuccess;
+  return ok ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
 int sage_debug_e4m3(const float* x, uint8_t* out, int64_t n, void* stream) {

@@ -20,6 +20,13 @@
 // The two tiles ping-pong: while one tile's softmax runs, the tensor core computes the other
 // tile's scores. Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 //
+// Variants (template argument PV): 0 = E4M3 P and V on kind::f8f6f4; 1 = the FP16 P·V
+// variant (P and V' in fp16 on kind::f16); 2 = the FP4 microscaled variant (pwwt.cn guide
+// §5.5): Q, K, V arrive as fp16 carriers of E2M1 codes x E4M3 block scales, and the softmax
+// quantises P the same way per 16 keys (scale = e4m3 of the block's largest 448 p,
+// codes = e2m1(448 p . fl32(6 / scale))); both products run on kind::f16, where every carrier
+// product is exact.
+//
 // Every wait is bounded; a timeout records SAGE_ERR_TIMEOUT and all roles exit cleanly.
 #include "launch.h"
 #include "problem.cuh"
@@ -55,7 +62,8 @@ struct AttnCfg {
   static constexpr int kOffBar = kOffP + 2 * kPBufs * kPTileBytes;
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kOffRho = kOffMisc + 64;  // FP4: fl32(6 / s) per E4M3 code s (128)
+  static constexpr int kBytes = kOffRho + 128 * 4;
   // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
   static constexpr int kSmem = (kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024);
   static_assert(kBytes + 1024 <= 232448, "shared memory budget");
@@ -180,11 +188,36 @@ __device__ __forceinline__ uint32_t pack_p2(float lo, float hi) {
   }
 }
 
+// Largest of 16 values.
+__device__ __forceinline__ float max16(const float (&e)[16]) {
+  float m = max3(e[0], e[1], e[2]);
+#pragma unroll
+  for (int u = 3; u < 15; u += 2) m = max3(m, e[u], e[u + 1]);
+  return fmaxf(m, e[15]);
+}
+
+// FP4 carriers of one 16-key group of y = 448 p values (y >= 0): the block scale is the
+// E4M3 rounding of the group's largest y, the codes e2m1(fl32(y . fl32(6 / scale))); rho_tab
+// holds fl32(6 / s) for every non-negative E4M3 code s.
+__device__ __forceinline__ void fp4_p_group(const float (&e)[16], const float* rho_tab,
+                                            uint32_t (&w)[8]) {
+  const uint32_t code = pack_e4m3x2(max16(e), 0.f);
+  const __half2 s2 = e4m3x2_to_half2((code & 0xffu) * 0x101u);
+  const float rho = rho_tab[code & 0x7fu];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float z0, z1;
+    mul2(z0, z1, e[2 * k], e[2 * k + 1], rho, rho);
+    w[k] = fp4_carrier2(z0, z1, s2);
+  }
+}
+
 // P~ = fmt(2^(S*c + bias)) for keys [0, limit) (0 beyond), written to the row's swizzled
 // P buffer; returns the row sum of the unquantised values.
-template <bool PV16>
+template <int PV>
 __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, float bias,
-                                              uint8_t* my_p, int r) {
+                                              uint8_t* my_p, int r, const float* rho_tab) {
+  constexpr bool PV16 = PV != 0;
   float a0 = 0.f, a1 = 0.f;
 #pragma unroll 1
   for (int ch = 0; ch < 4; ++ch) {
@@ -195,21 +228,36 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
     for (int half = 0; half < 2; ++half) {
       const float cgc = pick8(cg.v, 2 * ch + half);
       uint32_t w[PV16 ? 8 : 4];
+      if constexpr (PV == 2) {
+        float e[16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float e[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int u = half * 16 + q4 * 4 + v;
-          e[v] = ch * 32 + u < limit ? ex2(fmaf(__uint_as_float(t[u]), cgc, bias)) : 0.f;
+        for (int u = 0; u < 16; ++u) {
+          const int uu = half * 16 + u;
+          e[u] = ch * 32 + uu < limit ? ex2(fmaf(__uint_as_float(t[uu]), cgc, bias)) : 0.f;
         }
-        add2(a0, a1, a0, a1, e[0], e[1]);
-        add2(a0, a1, a0, a1, e[2], e[3]);
-        if constexpr (PV16) {
-          w[2 * q4] = pack_p2<true>(e[0], e[1]);
-          w[2 * q4 + 1] = pack_p2<true>(e[2], e[3]);
-        } else {
-          w[q4] = pack_p2<false>(e[0], e[1]) | (pack_p2<false>(e[2], e[3]) << 16);
+#pragma unroll
+        for (int u = 0; u < 16; u += 4) {
+          add2(a0, a1, a0, a1, e[u], e[u + 1]);
+          add2(a0, a1, a0, a1, e[u + 2], e[u + 3]);
+        }
+        fp4_p_group(e, rho_tab, w);
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float e[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int u = half * 16 + q4 * 4 + v;
+            e[v] = ch * 32 + u < limit ? ex2(fmaf(__uint_as_float(t[u]), cgc, bias)) : 0.f;
+          }
+          add2(a0, a1, a0, a1, e[0], e[1]);
+          add2(a0, a1, a0, a1, e[2], e[3]);
+          if constexpr (PV16) {
+            w[2 * q4] = pack_p2<true>(e[0], e[1]);
+            w[2 * q4 + 1] = pack_p2<true>(e[2], e[3]);
+          } else {
+            w[q4] = pack_p2<false>(e[0], e[1]) | (pack_p2<false>(e[2], e[3]) << 16);
+          }
         }
       }
       store_p_group<PV16>(my_p, r, 2 * ch + half, w);
@@ -224,10 +272,12 @@ __device__ __forceinline__ void trace(const Problem& p, bool on, int role, int t
     p.dbg_trace[(role * kTraceTiles + tile) * kTraceEvents + ev] = clock64();
 }
 
-template <int DP, bool PV16>
+template <int DP, int PV>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Problem p) {
+  constexpr bool PV16 = PV != 0;  // P·V on kind::f16 (fp16 P and V^T)
+  constexpr bool FP4 = PV == 2;
   using C = AttnCfg<DP, PV16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -248,6 +298,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* o_ready = o_full + 2;            // [2]
   uint64_t* drain = o_ready + 2;             // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  float* rho_tab = reinterpret_cast<float*>(sm + C::kOffRho);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,6 +337,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (FP4 && threadIdx.x < 128) {
+    // fl32(6 / s) for the non-negative E4M3 codes (0 for s = 0 and for the NaN code)
+    const float sv = __low2float(e4m3x2_to_half2(threadIdx.x * 0x101u));
+    rho_tab[threadIdx.x] = (sv > 0.f && threadIdx.x != 0x7f) ? __fdiv_rn(6.0f, sv) : 0.f;
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -466,11 +522,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const bool row_valid = active_tile && r < xrows;
     // sigma_P: 448 (the largest E4M3 magnitude) for E4M3 P in every accumulation mode, 1 for
     // fp16 P
-    const float log2_sigma = PV16 ? 0.0f : 8.807354922057604f;  // log2(448)
+    const float log2_sigma = (PV16 && !FP4) ? 0.0f : 8.807354922057604f;  // log2(448)
     const bool trs = tr && (warp & 3) == 0 && lane == 0;
     float sq = 0.f;
     if (row_valid) sq = __ldg(&p.sq[plane_q * p.sq_pp + (s.row0_q + i) / p.gq]);
-    const float row_scale = sq * p.sm_scale * kLog2e;
+    // FP4: the carriers are ~6x the mapped values on both sides, so the scores carry 36
+    const float row_scale = sq * p.sm_scale * (FP4 ? kLog2e / 36.0f : kLog2e);
     const float* skp = p.sk + plane_kv * p.sk_pp + (s.row0_k >> p.lgk);
     const int lgk = p.lgk;  // log2 of the K scale group (16 or 64 keys)
     float m = __int_as_float(0xff800000);  // running max (log2 units)
@@ -556,6 +613,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int g = 0; g < 8; ++g) {
             float a0 = 0.f, a1 = 0.f;
             uint32_t w[PV16 ? 8 : 4];
+            float eg[FP4 ? 16 : 1];  // FP4: the group's values, quantised once all are known
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int c = g * 16 + q4 * 4;
@@ -567,13 +625,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
               add2(a0, a1, a0, a1, e0, e1);
               add2(a0, a1, a0, a1, e2, e3);
-              if constexpr (PV16) {
+              if constexpr (FP4) {
+                eg[4 * q4] = e0; eg[4 * q4 + 1] = e1; eg[4 * q4 + 2] = e2; eg[4 * q4 + 3] = e3;
+              } else if constexpr (PV16) {
                 w[2 * q4] = pack_p2<true>(e0, e1);
                 w[2 * q4 + 1] = pack_p2<true>(e2, e3);
               } else {
                 w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
               }
             }
+            if constexpr (FP4) fp4_p_group(eg, rho_tab, w);
             store_p_group<PV16>(my_p, r, g, w);
             add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
           }
@@ -581,7 +642,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           Mult8 c8;
 #pragma unroll
           for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
-          gsum[0] = masked_tile_exp<PV16>(tS, limit, c8, bias, my_p, r);
+          gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
         // next tile's K scales (used one tile from now)
@@ -657,7 +718,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (n_tiles - 1) & 1, abort_flag));
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.0f / l;
+        // FP4: O = acc . s_v / (36 l) (both P·V carriers are ~6x their mapped values)
+        const float inv_l = 1.0f / (FP4 ? 36.0f * l : l);
 #pragma unroll 1
         for (int cc = 0; cc < DP / 32 && cc * 32 < p.d; ++cc) {
           uint32_t o[32];
@@ -743,22 +805,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-template <int DP, bool PV16>
+template <int DP, int PV>
 static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
-  constexpr int smem = AttnCfg<DP, PV16>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = AttnCfg<DP, PV != 0>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_kernel<DP, PV16>, grid, dim3(kAttnThreads), smem, stream, maps[0], maps[1],
+  return launch_pdl(attn_kernel<DP, PV>, grid, dim3(kAttnThreads), smem, stream, maps[0], maps[1],
                     maps[2], p);
 }
 
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
                              cudaStream_t stream) {
   const dim3 grid(p.hq, grid_pairs, p.batch);
-  if (p.pv16) return p.dp == 64 ? launch_attn_t<64, true>(p, maps, grid, stream)
-                                : launch_attn_t<128, true>(p, maps, grid, stream);
-  return p.dp == 64 ? launch_attn_t<64, false>(p, maps, grid, stream)
-                    : launch_attn_t<128, false>(p, maps, grid, stream);
+  if (p.fp4) return p.dp == 64 ? launch_attn_t<64, 2>(p, maps, grid, stream)
+                               : launch_attn_t<128, 2>(p, maps, grid, stream);
+  if (p.pv16) return p.dp == 64 ? launch_attn_t<64, 1>(p, maps, grid, stream)
+                                : launch_attn_t<128, 1>(p, maps, grid, stream);
+  return p.dp == 64 ? launch_attn_t<64, 0>(p, maps, grid, stream)
+                    : launch_attn_t<128, 0>(p, maps, grid, stream);
 }
 
 }  // namespace sage

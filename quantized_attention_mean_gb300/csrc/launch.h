@@ -36,6 +36,11 @@ cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, in
 cudaError_t launch_export_vt(const uint8_t* vt, int64_t pitch, int dp, int d, int planes, int n,
                              uint8_t* out, cudaStream_t st);
 cudaError_t launch_e4m3(const float* x, uint8_t* out, int64_t n, cudaStream_t st);
+cudaError_t launch_e2m1(const float* x, uint8_t* out, int64_t n, cudaStream_t st);
+cudaError_t launch_export_fp16(const __half* codes, int64_t rows_pp, int dp, int d, int planes,
+                               int n, uint16_t* out, cudaStream_t st);
+cudaError_t launch_export_vt16(const __half* vt, int64_t pitch, int dp, int d, int planes, int n,
+                               uint16_t* out, cudaStream_t st);
 // Short-sequence kernel: one launch for the whole forward of a dense problem with at most
 // kShortMaxKeys keys and kShortMaxQueries queries (statistics, quantisation and attention per
 // CTA of 128 query rows; short.cu). Selected with sage_debug_select_path(2).

@@ -25,7 +25,9 @@ struct Problem {
   int varlen, dtype, is_causal, return_lse, smooth_k, smooth_v;
   int gq, gk, lgk;                 // token-group sizes of Q and K scales; lgk = log2(gk)
   int vec16;                       // inputs allow 16-byte vector loads
-  int pv16;                        // FP16 P·V variant: V^T stored as fp16, P in fp16
+  int pv16;                        // P·V on fp16 operands: V^T stored as fp16, P in fp16
+  int fp4;                         // FP4 microscaled variant (with pv16): Q, K, V, P carried
+                                   // as E2M1 code x E4M3 block scale in fp16
   float sm_scale;
   float range_limit;               // smallest float >= 2^38 / N (dense only; varlen per seq)
   const void* q; int64_t q_sb, q_sh, q_sn;
@@ -129,6 +131,43 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ---- FP4 microscaling (pwwt.cn guide §5.5, SageAttention3 "FP4 microscaling"): E2M1
+// elements, one E4M3 scale per block of 16 along the dot-product dimension. A block's scale
+// s is its largest mapped magnitude rounded to E4M3; each element is coded as
+// e2m1(fl32(u · fl32(6 / s))) and enters the tensor cores as its carrier code · s, which fp16
+// holds exactly (at most 5 significant bits, between 2^-10 and 2688).
+
+// E4M3 block scale of a block maximum m >= 0: its value as an fp16 pair (both halves) and
+// rho = fl32(6 / s) (0 when s = 0).
+struct Fp4Scale {
+  __half2 s2;
+  float rho;
+};
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t codes16) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(codes16)));
+  return *reinterpret_cast<__half2*>(&h);
+}
+__device__ __forceinline__ Fp4Scale fp4_block_scale(float m) {
+  Fp4Scale r;
+  r.s2 = e4m3x2_to_half2(pack_e4m3x2(m, m));
+  const float s = __low2float(r.s2);
+  r.rho = s > 0.f ? __fdiv_rn(6.0f, s) : 0.f;
+  return r;
+}
+// Two already scaled values z = fl32(u · rho) to their E2M1 codes (RNE, saturating at ±6) and
+// back as an fp16 pair, times the pair's block scales s2: the two carriers, z0 in the low half.
+__device__ __forceinline__ uint32_t fp4_carrier2(float z0, float z1, __half2 s2) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h)
+      : "f"(z1), "f"(z0));
+  const __half2 c = __hmul2(*reinterpret_cast<const __half2*>(&h), s2);  // exact
+  return *reinterpret_cast<const uint32_t*>(&c);
 }
 
 // Order-preserving float -> unsigned map (a larger float has a larger code, and every

@@ -242,13 +242,15 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
   const float amax = fmaxf(fabsf(mx), fabsf(mn));
   p.kmean[i] = km;
   p.vmean[i] = vm;
-  // the FP16 P·V variant keeps V' unscaled
-  p.vscale[i] = p.pv16 ? 1.0f : (amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f);
-  p.vrcp[i] = p.pv16 ? 1.0f : (amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f);
+  // the FP16 P·V variant keeps V' unscaled; the FP8 and FP4 ones map absmax onto 448
+  const bool unscaled = p.pv16 && !p.fp4;
+  p.vscale[i] = unscaled ? 1.0f : (amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f);
+  p.vrcp[i] = unscaled ? 1.0f : (amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f);
 }
 
 // ------------------------------------------------------------------------------------------
-// Quantisation, one instantiation per tensor (kind 0 = Q, 1 = K, 2 = V). Grid: (128-token
+// Quantisation, one instantiation per tensor (kind 0 = Q, 1 = K, 2 = V, 3 = V in fp16;
+// FP4 variant: 4 = Q, 5 = K, 6 = V). Grid: (128-token
 // tiles, heads, batch). NT threads; thread (rg, vec) holds rows rg + RG*i (i < 128 / RG,
 // RG = NT / TPR), channels [8*vec, 8*vec + 8). NT is 512 for dense problems at padded
 // head_dim 128 (4 rows per thread: less unrolled code per warp than 8 rows at 256 threads,
@@ -260,13 +262,18 @@ __global__ void kv_finalize_kernel(Problem p, int n_stats) {
 //   V: V' = V - vmean, E4M3 with the per-channel scale absmax/448, written transposed
 //      [channel][token] so that P.V reads V^T tiles K-major.
 //   V (kind 3, FP16 P·V variant): V' = V - vmean rounded to fp16 (RNE), transposed likewise.
+//   FP4 variant: Q and K' (kinds 4, 5) are mapped onto [-448, 448] by their token group's
+//      scale g = absmax/448 (u = fl32(x · fl32(448/absmax))) and microscaled in blocks of 16
+//      channels of a row; V' (kind 6) is mapped by its channel's scale (as for FP8) and
+//      microscaled in blocks of 16 tokens of a channel, transposed like kind 3. Each element
+//      is stored as its fp16 carrier (E2M1 code x E4M3 block scale).
 // Rows past the sequence end up to the stored tile end are written as zeros.
 template <typename T, int kind, int TPR, int NT>
 __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, int b) {
   constexpr int RG = NT / TPR;       // row groups
   constexpr int RPT = kTileRows / RG;  // rows per thread
   const Seq s = get_seq(p, b);
-  const int len = kind == 0 ? s.len_q : s.len_k;
+  const int len = (kind == 0 || kind == 4) ? s.len_q : s.len_k;
   // rows stored for this sequence: dense planes hold exactly len rows; varlen segments are
   // padded to a multiple of 128
   const int stored = p.varlen ? (len + kTileRows - 1) / kTileRows * kTileRows : len;
@@ -275,7 +282,7 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
   const int vec = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = vec * 8;
   const int d = p.d, dp = p.dp;
-  const int hk = kind == 0 ? h / (p.hq / p.hkv) : h;   // kv head feeding this q head
+  const int hk = (kind == 0 || kind == 4) ? h / (p.hq / p.hkv) : h;  // kv head of this q head
   const int64_t sidx = ((int64_t)b * p.hkv + hk) * d;
 
   __shared__ float rowmax[kTileRows];
@@ -283,14 +290,15 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 
   // per-channel values from the finalize pass: smoothing means, V scale reciprocals, and for
   // Q heads the K mean used by the LSE term
+  constexpr bool kIsQ = kind == 0 || kind == 4, kIsK = kind == 1 || kind == 5;
+  constexpr bool kIsV = !kIsQ && !kIsK;
   float mean[8], rcpv[8], kmean_q[8];
-  const bool want_qkc = kind == 0 && p.return_lse && p.smooth_k;
+  const bool want_qkc = kIsQ && p.return_lse && p.smooth_k;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const bool ch = c0 + i < d;
-    mean[i] = (ch && kind == 1) ? p.kmean[sidx + c0 + i]
-                                : ((ch && kind >= 2) ? p.vmean[sidx + c0 + i] : 0.f);
-    rcpv[i] = (ch && kind == 2) ? p.vrcp[sidx + c0 + i] : 0.f;
+    mean[i] = (ch && kIsK) ? p.kmean[sidx + c0 + i] : ((ch && kIsV) ? p.vmean[sidx + c0 + i] : 0.f);
+    rcpv[i] = (ch && (kind == 2 || kind == 6)) ? p.vrcp[sidx + c0 + i] : 0.f;
     kmean_q[i] = (ch && want_qkc) ? p.kmean[sidx + c0 + i] : 0.f;
   }
 
@@ -298,14 +306,14 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
   // 0); every row of the thread is requested before any is used
   const T* base;
   int64_t sn;
-  if (kind == 0) {
+  if (kIsQ) {
     base = static_cast<const T*>(p.q) + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh; sn = p.q_sn;
-  } else if (kind == 1) {
+  } else if (kIsK) {
     base = static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)h * p.k_sh; sn = p.k_sn;
   } else {
     base = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)h * p.v_sh; sn = p.v_sn;
   }
-  const int tok0 = kind == 0 ? s.tok0_q : s.tok0_k;
+  const int tok0 = kIsQ ? s.tok0_q : s.tok0_k;
   uint4 raw[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
@@ -321,18 +329,61 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     for (int j = 0; j < 8; ++j) x[j] = (live && c0 + j < d) ? __fsub_rn(x[j], mean[j]) : 0.f;
   };
 
-  if constexpr (kind == 3) {
-    // ---- V: fp16 values, transposed through shared memory. Element (channel c, token rr)
-    // sits at column rr ^ (8 * ((c >> 3) & 15)): whole 16-byte units move, and the 16 threads
-    // of a row (one channel octet each) hit different banks.
+  if constexpr (kind == 3 || kind == 6) {
+    // ---- V: fp16 values (kind 3) or FP4 carriers (kind 6), transposed through shared
+    // memory. Element (channel c, token rr) sits at column rr ^ (8 * ((c >> 3) & 15)): whole
+    // 16-byte units move, and the 16 threads of a row (one channel octet each) hit different
+    // banks.
     __shared__ __align__(16) __half vtile16[128][kTileRows];
+    if constexpr (kind == 6) {
+      // block maxima of |u| per (16-token block, channel), then each block's scale and rho
+      __shared__ unsigned bmax[kTileRows / 16][128];
+      __shared__ float brho[kTileRows / 16][128];
+      __shared__ __half bscale[kTileRows / 16][128];
+      for (int idx = threadIdx.x; idx < (kTileRows / 16) * 128; idx += NT) bmax[idx >> 7][idx & 127] = 0u;
+      __syncthreads();
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int rr = rg + RG * i;
-      float x[8];
-      row_values(i, x);
+      for (int i = 0; i < RPT; ++i) {
+        const int rr = rg + RG * i;
+        float x[8];
+        row_values(i, x);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) vtile16[c0 + j][rr ^ ((vec & 15) << 3)] = __float2half_rn(x[j]);
+        for (int j = 0; j < 8; ++j)
+          if (c0 + j < dp) atomicMax(&bmax[rr >> 4][c0 + j], __float_as_uint(fabsf(__fmul_rn(x[j], rcpv[j]))));
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < (kTileRows / 16) * dp; idx += NT) {
+        const int blk = idx / dp, c = idx - blk * dp;
+        const Fp4Scale sc = fp4_block_scale(__uint_as_float(bmax[blk][c]));
+        brho[blk][c] = sc.rho;
+        bscale[blk][c] = __low2half(sc.s2);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int rr = rg + RG * i;
+        float x[8];
+        row_values(i, x);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const float z0 = __fmul_rn(__fmul_rn(x[j], rcpv[j]), brho[rr >> 4][c0 + j]);
+          const float z1 = __fmul_rn(__fmul_rn(x[j + 1], rcpv[j + 1]), brho[rr >> 4][c0 + j + 1]);
+          const uint32_t two = fp4_carrier2(z0, z1, __halves2half2(bscale[rr >> 4][c0 + j],
+                                                                    bscale[rr >> 4][c0 + j + 1]));
+          const __half2 h2 = *reinterpret_cast<const __half2*>(&two);
+          vtile16[c0 + j][rr ^ ((vec & 15) << 3)] = __low2half(h2);
+          vtile16[c0 + j + 1][rr ^ ((vec & 15) << 3)] = __high2half(h2);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int rr = rg + RG * i;
+        float x[8];
+        row_values(i, x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) vtile16[c0 + j][rr ^ ((vec & 15) << 3)] = __float2half_rn(x[j]);
+      }
     }
     __syncthreads();
     const int64_t plane = plane_of(p, b, h, p.hkv);
@@ -382,8 +433,10 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     return;
   }
 
-  // ---- Q / K: INT8 codes per token group
-  const int gs = kind == 0 ? p.gq : p.gk;
+  // ---- Q / K: INT8 codes (kinds 0, 1) or FP4 carriers (kinds 4, 5) per token group
+  constexpr bool kFp4 = kind >= 4;
+  constexpr float kRange = kFp4 ? 448.0f : 127.0f;  // the group's absmax maps onto this
+  const int gs = kIsQ ? p.gq : p.gk;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     float x[8];
@@ -396,8 +449,8 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     if (vec == 0) rowmax[rg + RG * i] = a;
   }
   __syncthreads();
-  const int64_t plane = plane_of(p, b, h, kind == 0 ? p.hq : p.hkv);
-  const int row0 = kind == 0 ? s.row0_q : s.row0_k;
+  const int64_t plane = plane_of(p, b, h, kIsQ ? p.hq : p.hkv);
+  const int row0 = kIsQ ? s.row0_q : s.row0_k;
   {
     // group absmax: warps 0-3 each own 32 consecutive rows; groups of <= 32 rows reduce with
     // shuffles, groups of 64 / 128 rows combine the per-warp maxima
@@ -420,17 +473,17 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     const int r = warp * 32 + lane;  // row of this lane (warps 0-3)
     if (warp < 4 && r % gs == 0) {
       const int g = r / gs;
-      grcp[g] = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
+      grcp[g] = a > 0.f ? __fdiv_rn(kRange, a) : 0.f;
       if (r0 + r < len) {
-        float* sc = kind == 0 ? p.sq : p.sk;
-        const int64_t pp = kind == 0 ? p.sq_pp : p.sk_pp;
-        sc[plane * pp + (row0 + r0) / gs + g] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+        float* sc = kIsQ ? p.sq : p.sk;
+        const int64_t pp = kIsQ ? p.sq_pp : p.sk_pp;
+        sc[plane * pp + (row0 + r0) / gs + g] = a > 0.f ? __fdiv_rn(a, kRange) : 0.f;
       }
     }
   }
   __syncthreads();
-  __half* codes = kind == 0 ? p.qc : p.kc;
-  const int64_t rows_pp = kind == 0 ? p.q_rows : p.k_rows;
+  __half* codes = kIsQ ? p.qc : p.kc;
+  const int64_t rows_pp = kIsQ ? p.q_rows : p.k_rows;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     const int rr = rg + RG * i;
@@ -439,14 +492,32 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     float x[8];
     row_values(i, x);
     __align__(16) __half2 hv[4];
+    if constexpr (kFp4) {
+      // u = fl32(x * r); the 16-channel block of this row spans this thread and its
+      // neighbour (vec ^ 1)
+      float u[8], m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      // rint_even(fl32(x * r)) via the rounding constant (|x * r| <= 127.00002 < 2^22)
-      float c0 = __fsub_rn(__fadd_rn(__fmul_rn(x[j], rc), kRoundMagic), kRoundMagic);
-      float c1 = __fsub_rn(__fadd_rn(__fmul_rn(x[j + 1], rc), kRoundMagic), kRoundMagic);
-      c0 = fminf(fmaxf(c0, -127.0f), 127.0f);
-      c1 = fminf(fmaxf(c1, -127.0f), 127.0f);
-      hv[j / 2] = __floats2half2_rn(c0, c1);  // exact: integers of magnitude <= 127
+      for (int j = 0; j < 8; ++j) {
+        u[j] = __fmul_rn(x[j], rc);
+        m = fmaxf(m, fabsf(u[j]));
+      }
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const Fp4Scale sc = fp4_block_scale(m);
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const uint32_t two = fp4_carrier2(__fmul_rn(u[j], sc.rho), __fmul_rn(u[j + 1], sc.rho), sc.s2);
+        hv[j / 2] = *reinterpret_cast<const __half2*>(&two);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        // rint_even(fl32(x * r)) via the rounding constant (|x * r| <= 127.00002 < 2^22)
+        float c0 = __fsub_rn(__fadd_rn(__fmul_rn(x[j], rc), kRoundMagic), kRoundMagic);
+        float c1 = __fsub_rn(__fadd_rn(__fmul_rn(x[j + 1], rc), kRoundMagic), kRoundMagic);
+        c0 = fminf(fmaxf(c0, -127.0f), 127.0f);
+        c1 = fminf(fmaxf(c1, -127.0f), 127.0f);
+        hv[j / 2] = __floats2half2_rn(c0, c1);  // exact: integers of magnitude <= 127
+      }
     }
     if (c0 < dp && r < stored)
       *reinterpret_cast<uint4*>(codes + (plane * rows_pp + row0 + r) * dp + c0) =
@@ -464,14 +535,15 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 
 // Q, K and V quantisation in one launch. Grid: (128-token tiles of the longest sequence,
 // Hq + 2 Hkv, batch): blockIdx.y selects a Q head, then a K head, then a V head.
-template <typename T, int TPR, bool PV16, int NT>
+// VM: 0 = FP8 V, 1 = fp16 V (FP16 P·V variant), 2 = FP4 microscaled Q, K and V.
+template <typename T, int TPR, int VM, int NT>
 __global__ void __launch_bounds__(NT, NT == 512 ? 2 : (TPR == 8 ? 4 : 3)) quant_kernel(Problem p) {
   pdl_trigger();
   pdl_wait();  // the finalisation's means and scales
   const int y = blockIdx.y;
-  if (y < p.hq) quant_block<T, 0, TPR, NT>(p, blockIdx.x, y, blockIdx.z);
-  else if (y < p.hq + p.hkv) quant_block<T, 1, TPR, NT>(p, blockIdx.x, y - p.hq, blockIdx.z);
-  else quant_block<T, PV16 ? 3 : 2, TPR, NT>(p, blockIdx.x, y - p.hq - p.hkv, blockIdx.z);
+  if (y < p.hq) quant_block<T, VM == 2 ? 4 : 0, TPR, NT>(p, blockIdx.x, y, blockIdx.z);
+  else if (y < p.hq + p.hkv) quant_block<T, VM == 2 ? 5 : 1, TPR, NT>(p, blockIdx.x, y - p.hq, blockIdx.z);
+  else quant_block<T, VM == 0 ? 2 : (VM == 1 ? 3 : 6), TPR, NT>(p, blockIdx.x, y - p.hq - p.hkv, blockIdx.z);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -494,6 +566,36 @@ __global__ void export_vt_kernel(const uint8_t* vt, int64_t pitch, int dp, int d
     const int c = (int)(i % d);
     const int64_t r = (i / d) % n, pl = i / ((int64_t)d * n);
     out[i] = vt[(pl * dp + c) * pitch + r];
+  }
+}
+__global__ void export_fp16_kernel(const __half* codes, int64_t rows_pp, int dp, int d,
+                                   int planes, int n, uint16_t* out) {
+  const int64_t total = (int64_t)planes * n * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % d);
+    const int64_t r = (i / d) % n, pl = i / ((int64_t)d * n);
+    out[i] = __half_as_ushort(codes[(pl * rows_pp + r) * dp + c]);
+  }
+}
+__global__ void export_vt16_kernel(const __half* vt, int64_t pitch, int dp, int d, int planes,
+                                   int n, uint16_t* out) {
+  const int64_t total = (int64_t)planes * n * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % d);
+    const int64_t r = (i / d) % n, pl = i / ((int64_t)d * n);
+    out[i] = __half_as_ushort(vt[(pl * dp + c) * pitch + r]);
+  }
+}
+__global__ void e2m1_kernel(const float* x, uint8_t* out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint16_t c;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(c)
+        : "f"(0.f), "f"(x[i]));
+    out[i] = static_cast<uint8_t>(c & 0xF);
   }
 }
 __global__ void e4m3_kernel(const float* x, uint8_t* out, int64_t n) {
@@ -534,15 +636,19 @@ template <typename T>
 static cudaError_t launch_quant_t(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st) {
   const int len = max_len_q > max_len_k ? max_len_q : max_len_k;
   const dim3 grid((len + kTileRows - 1) / kTileRows, p.hq + 2 * p.hkv, p.batch);
+  const int vm = p.fp4 ? 2 : (p.pv16 ? 1 : 0);
   if (p.dp == 64) {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 8, true, 256>, grid, dim3(256), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 8, false, 256>, grid, dim3(256), 0, st, p);
+    return vm == 2 ? launch_pdl(quant_kernel<T, 8, 2, 256>, grid, dim3(256), 0, st, p)
+         : vm == 1 ? launch_pdl(quant_kernel<T, 8, 1, 256>, grid, dim3(256), 0, st, p)
+                   : launch_pdl(quant_kernel<T, 8, 0, 256>, grid, dim3(256), 0, st, p);
   } else if (!p.varlen) {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true, 512>, grid, dim3(512), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 16, false, 512>, grid, dim3(512), 0, st, p);
+    return vm == 2 ? launch_pdl(quant_kernel<T, 16, 2, 512>, grid, dim3(512), 0, st, p)
+         : vm == 1 ? launch_pdl(quant_kernel<T, 16, 1, 512>, grid, dim3(512), 0, st, p)
+                   : launch_pdl(quant_kernel<T, 16, 0, 512>, grid, dim3(512), 0, st, p);
   } else {
-    return p.pv16 ? launch_pdl(quant_kernel<T, 16, true, 256>, grid, dim3(256), 0, st, p)
-                  : launch_pdl(quant_kernel<T, 16, false, 256>, grid, dim3(256), 0, st, p);
+    // the FP4 variant has no varlen entry point
+    return vm == 1 ? launch_pdl(quant_kernel<T, 16, 1, 256>, grid, dim3(256), 0, st, p)
+                   : launch_pdl(quant_kernel<T, 16, 0, 256>, grid, dim3(256), 0, st, p);
   }
 }
 
@@ -561,6 +667,23 @@ cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, in
 cudaError_t launch_export_vt(const uint8_t* vt, int64_t pitch, int dp, int d, int planes, int n,
                              uint8_t* out, cudaStream_t st) {
   export_vt_kernel<<<1024, 256, 0, st>>>(vt, pitch, dp, d, planes, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e2m1(const float* x, uint8_t* out, int64_t n, cudaStream_t st) {
+  e2m1_kernel<<<1024, 256, 0, st>>>(x, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_fp16(const __half* codes, int64_t rows_pp, int dp, int d, int planes,
+                               int n, uint16_t* out, cudaStream_t st) {
+  export_fp16_kernel<<<1024, 256, 0, st>>>(codes, rows_pp, dp, d, planes, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_vt16(const __half* vt, int64_t pitch, int dp, int d, int planes, int n,
+                               uint16_t* out, cudaStream_t st) {
+  export_vt16_kernel<<<1024, 256, 0, st>>>(vt, pitch, dp, d, planes, n, out);
   return cudaGetLastError();
 }
 

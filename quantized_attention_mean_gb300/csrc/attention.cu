@@ -266,13 +266,19 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
   return a0 + a1;
 }
 
-// Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0).
+// Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0). Only
+// the tracing instantiation of the kernel (ON = true) contains the records: a runtime check at
+// every trace point split the softmax loop into basic blocks the compiler could not schedule
+// across (measured: 6% of the attention time at head_dim 64, 9% at 128).
+template <bool ON>
 __device__ __forceinline__ void trace(const Problem& p, bool on, int role, int tile, int ev) {
-  if (on && tile < kTraceTiles)
-    p.dbg_trace[(role * kTraceTiles + tile) * kTraceEvents + ev] = clock64();
+  if constexpr (ON) {
+    if (on && tile < kTraceTiles)
+      p.dbg_trace[(role * kTraceTiles + tile) * kTraceEvents + ev] = clock64();
+  }
 }
 
-template <int DP, int PV>
+template <int DP, int PV, bool TRACE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Problem p) {
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool tr = p.dbg_trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  const bool tr = TRACE && p.dbg_trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   // ---- work item: (query head, 256-row pair, sequence); heaviest pairs first when causal
   const int h = blockIdx.x;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int st = j % C::kKStages;
         if (j >= C::kKStages) ok = mbar_wait(&k_empty[st], ((j / C::kKStages) - 1) & 1, abort_flag);
         if (!ok) break;
-        trace(p, tr, 3, j, 0);
+        trace<TRACE>(p, tr, 3, j, 0);
         mbar_arrive_expect_tx(&k_full[st], C::kKTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sK + st * C::kKTileBytes + c * kTileKeys * 128, &tmK, &k_full[st], c * 64,
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sv = j % C::kVStages;
         if (j >= C::kVStages) ok = mbar_wait(&v_empty[sv], ((j / C::kVStages) - 1) & 1, abort_flag);
         if (!ok) break;
-        trace(p, tr, 3, j, 1);
+        trace<TRACE>(p, tr, 3, j, 1);
         mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
         if constexpr (PV16) {
           // fp16 V^T: two 64-key chunks of DP rows x 128 bytes
@@ -476,7 +482,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // S_j(x) consumed and P_j(x) written: the tile's next scores can start right away
           ok = wait_all(&p_full[x], j & 1);
           if (!ok) break;
-          trace(p, tr_mma, 2, j, 4 * x + 0);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
           tc_fence_after();
           if (j + 1 < n_tiles) {
             if (x == 0) ok = wait_all(&k_full[nst], ((j + 1) / C::kKStages) & 1);
@@ -484,16 +490,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             issue_qk(x, nst);
           }
-          trace(p, tr_mma, 2, j, 4 * x + 1);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
           // O(x) rescaled for the new running max: accumulate P_j(x) V_j
           ok = wait_all(&o_ready[x], j & 1);
           if (!ok) break;
-          trace(p, tr_mma, 2, j, 4 * x + 2);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
           if (x == 0) ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_pv(x, sv, j % C::kPBufs, j == 0);
-          trace(p, tr_mma, 2, j, 4 * x + 3);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
         }
         if (!ok) break;
         if (j + 1 < n_tiles) mma_commit_warp(&k_empty[nst]);
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
         if (!ok) break;
-        trace(p, trs, x, j, 0);
+        trace<TRACE>(p, trs, x, j, 0);
         tc_fence_after();
         const int kv0 = j * kTileKeys;
         const int limit = row_limit - kv0;  // this row's allowed keys in the tile: [0, limit)
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_wait_ld(sr[1]);
           tmem_wait_ld(sr[2]);
           tmem_wait_ld(sr[3]);
-          trace(p, trs, x, j, 1);
+          trace<TRACE>(p, trs, x, j, 1);
           // max of the raw integer scores per sub-group (three-input max), then scaled
           // (c_g >= 0 keeps the order)
 #pragma unroll
@@ -586,9 +592,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
           tile_max = masked_tile_max(tS, limit, c8);
-          trace(p, trs, x, j, 1);
+          trace<TRACE>(p, trs, x, j, 1);
         }
-        trace(p, trs, x, j, 2);
+        trace<TRACE>(p, trs, x, j, 2);
         const float m_new = fmaxf(m, tile_max);
         const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
@@ -602,7 +608,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_after();
         }
         uint8_t* const my_p = p_row + (j % C::kPBufs) * C::kPTileBytes;
-        trace(p, trs, x, j, 4);
+        trace<TRACE>(p, trs, x, j, 4);
         // P~ = e4m3(2^(x - m) * sigma) written 16 keys (one 16-byte chunk, 128-byte swizzle)
         // at a time; the row sum uses four independent accumulator pairs
         float gsum[8];
@@ -645,19 +651,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
-        // next tile's K scales (used one tile from now)
+        // next tile's K scales (used one tile from now): two loads when a K scale group is
+        // 64 keys, eight when it is 16
+        if (lgk == 6) {
+          const int kg = kv0 + kTileKeys;
+          const float s0 = kg < s.len_k ? __ldg(&skp[kg >> 6]) : 0.f;
+          const float s1 = kg + 64 < s.len_k ? __ldg(&skp[(kg >> 6) + 1]) : 0.f;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int kg = kv0 + kTileKeys + g * 16;
-          skn[g] = kg < s.len_k ? __ldg(&skp[kg >> lgk]) : 0.f;
+          for (int g = 0; g < 8; ++g) skn[g] = g < 4 ? s0 : s1;
+        } else {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const int kg = kv0 + kTileKeys + g * 16;
+            skn[g] = kg < s.len_k ? __ldg(&skp[kg >> lgk]) : 0.f;
+          }
         }
-        trace(p, trs, x, j, 3);
+        trace<TRACE>(p, trs, x, j, 3);
         l = l * alpha + rs;
         m = m_new;
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
-        trace(p, trs, x, j, 5);
+        trace<TRACE>(p, trs, x, j, 5);
         // rescale this warp's O rows for the grown max while the next scores are computed;
         // P_j(x) V_j is issued only after o_ready. O holds the sum up to tile j - 1 once P.V
         // of tile j - 1 is complete.
@@ -690,7 +705,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&o_ready[x]);
-        trace(p, trs, x, j, 6);
+        trace<TRACE>(p, trs, x, j, 6);
       }
       // ---- epilogue: out = acc . s_v / l + v_mean, then the LSE. The output address, the LSE
       // term and the first chunk's V scales / means are fetched while P.V of the last tile
@@ -788,7 +803,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                       : ((int64_t)b * p.hq + h) * p.nq + i;
           p.lse[li] = lse;
         }
-        trace(p, trs, x, n_tiles - 1, 7);
+        trace<TRACE>(p, trs, x, n_tiles - 1, 7);
       }
       if (!ok) record_error(p.err, kDevTimeout);
     }
@@ -805,18 +820,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-template <int DP, int PV>
+template <int DP, int PV, bool TRACE = false>
 static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
   constexpr int smem = AttnCfg<DP, PV != 0>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_kernel<DP, PV>, grid, dim3(kAttnThreads), smem, stream, maps[0], maps[1],
-                    maps[2], p);
+  return launch_pdl(attn_kernel<DP, PV, TRACE>, grid, dim3(kAttnThreads), smem, stream, maps[0],
+                    maps[1], maps[2], p);
 }
 
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
                              cudaStream_t stream) {
   const dim3 grid(p.hq, grid_pairs, p.batch);
+  // the tracing instantiation exists for the E4M3 P·V kernel only
+  if (p.dbg_trace != nullptr && !p.pv16)
+    return p.dp == 64 ? launch_attn_t<64, 0, true>(p, maps, grid, stream)
+                      : launch_attn_t<128, 0, true>(p, maps, grid, stream);
   if (p.fp4) return p.dp == 64 ? launch_attn_t<64, 2>(p, maps, grid, stream)
                                : launch_attn_t<128, 2>(p, maps, grid, stream);
   if (p.pv16) return p.dp == 64 ? launch_attn_t<64, 1>(p, maps, grid, stream)

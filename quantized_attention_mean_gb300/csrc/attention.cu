@@ -266,10 +266,75 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
   return a0 + a1;
 }
 
+// P~ = fmt(2^(S * c_g + bias)) of every key of a fully visible tile whose scores sr are in
+// registers, written to the row's P buffer; the unquantised values are summed into gsum (four
+// independent accumulator pairs).
+template <int PV>
+__device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const float (&cg)[8],
+                                              float bias, uint8_t* my_p, int r,
+                                              const float* rho_tab, float (&gsum)[8]) {
+  constexpr bool PV16 = PV != 0, FP4 = PV == 2;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float a0 = 0.f, a1 = 0.f;
+    uint32_t w[PV16 ? 8 : 4];
+    float eg[FP4 ? 16 : 1];  // FP4: the group's values, quantised once all are known
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int c = g * 16 + q4 * 4;
+      float x0, x1, x2, x3;
+      fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
+           cg[g], cg[g], bias, bias);
+      fma2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
+           cg[g], cg[g], bias, bias);
+      const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+      add2(a0, a1, a0, a1, e0, e1);
+      add2(a0, a1, a0, a1, e2, e3);
+      if constexpr (FP4) {
+        eg[4 * q4] = e0; eg[4 * q4 + 1] = e1; eg[4 * q4 + 2] = e2; eg[4 * q4 + 3] = e3;
+      } else if constexpr (PV16) {
+        w[2 * q4] = pack_p2<true>(e0, e1);
+        w[2 * q4 + 1] = pack_p2<true>(e2, e3);
+      } else {
+        w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
+      }
+    }
+    if constexpr (FP4) fp4_p_group(eg, rho_tab, w);
+    store_p_group<PV16>(my_p, r, g, w);
+    add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
+  }
+}
+
+// Max over a fully visible tile of S * c_g, the scores loaded into registers sr.
+__device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32], const float (&cg)[8]) {
+  tmem_ld32(tS + 0, sr[0]);
+  tmem_ld32(tS + 32, sr[1]);
+  tmem_ld32(tS + 64, sr[2]);
+  tmem_ld32(tS + 96, sr[3]);
+  tmem_wait_ld(sr[0]);
+  tmem_wait_ld(sr[1]);
+  tmem_wait_ld(sr[2]);
+  tmem_wait_ld(sr[3]);
+  // max of the raw integer scores per sub-group (three-input max), then scaled (c_g >= 0
+  // keeps the order)
+  float tile_max = __int_as_float(0xff800000);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
+    float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+    for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    a = fmaxf(a, __uint_as_float(v[15]));
+    tile_max = fmaxf(tile_max, a * cg[g]);
+  }
+  return tile_max;
+}
+
 // Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0). Only
-// the tracing instantiation of the kernel (ON = true) contains the records: a runtime check at
-// every trace point split the softmax loop into basic blocks the compiler could not schedule
-// across (measured: 6% of the attention time at head_dim 64, 9% at 128).
+// the test instantiation of the kernel (ON = true: pipeline trace and integer-score dump)
+// contains the records: a runtime check at every trace point split the softmax loop into basic
+// blocks the compiler could not schedule across (measured: 6% of the attention time at
+// head_dim 64, 9% at 128).
 template <bool ON>
 __device__ __forceinline__ void trace(const Problem& p, bool on, int role, int tile, int ev) {
   if constexpr (ON) {
@@ -554,9 +619,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kv0 = j * kTileKeys;
         const int limit = row_limit - kv0;  // this row's allowed keys in the tile: [0, limit)
         const bool masked = __any_sync(0xffffffffu, limit < kTileKeys);
-        if (__builtin_expect(p.dbg_scores != nullptr, 0))
-          dump_scores_row(tS, row_valid, p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk + kv0,
-                          min(kTileKeys, s.len_k - kv0));
+        if constexpr (TRACE || DP == 128) {  // (head_dim 128: measured faster with the check)
+          if (p.dbg_scores != nullptr)
+            dump_scores_row(tS, row_valid, p.dbg_scores + ((int64_t)(b * p.hq + h) * p.nq + i) * p.nk + kv0,
+                            min(kTileKeys, s.len_k - kv0));
+        }
         // multipliers c_g = s_q * s_k * sm_scale * log2(e) for the 8 sub-groups of 16 keys
         // (a K scale group is 16 or 64 keys, so each sub-group has one scale)
         float cg[8];
@@ -564,91 +631,59 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int g = 0; g < 8; ++g) cg[g] = row_scale * skn[g];
         uint32_t sr[4][32];
         float tile_max = __int_as_float(0xff800000);
-        if (__builtin_expect(!masked, 1)) {
-          // every key of the tile is visible: scores stay in registers
-          tmem_ld32(tS + 0, sr[0]);
-          tmem_ld32(tS + 32, sr[1]);
-          tmem_ld32(tS + 64, sr[2]);
-          tmem_ld32(tS + 96, sr[3]);
-          tmem_wait_ld(sr[0]);
-          tmem_wait_ld(sr[1]);
-          tmem_wait_ld(sr[2]);
-          tmem_wait_ld(sr[3]);
-          trace<TRACE>(p, trs, x, j, 1);
-          // max of the raw integer scores per sub-group (three-input max), then scaled
-          // (c_g >= 0 keeps the order)
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
-            float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-            for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-            a = fmaxf(a, __uint_as_float(v[15]));
-            tile_max = fmaxf(tile_max, a * cg[g]);
-          }
-        } else {
-          // causal diagonal or ragged tail: keys past the row's limit excluded
-          Mult8 c8;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
-          tile_max = masked_tile_max(tS, limit, c8);
-          trace<TRACE>(p, trs, x, j, 1);
-        }
-        trace<TRACE>(p, trs, x, j, 2);
-        const float m_new = fmaxf(m, tile_max);
-        const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
-        const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
-        const float bias = log2_sigma - m_use;
-        // with one P buffer it is free once P.V of tile j - 1 has completed; with two, P.V of
-        // tile j - 2 (its previous reader) completed before this row's rescale wait of tile
-        // j - 1 below
-        if (C::kPBufs == 1 && j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-        }
+        float m_new, alpha, bias;
         uint8_t* const my_p = p_row + (j % C::kPBufs) * C::kPTileBytes;
-        trace<TRACE>(p, trs, x, j, 4);
-        // P~ = e4m3(2^(x - m) * sigma) written 16 keys (one 16-byte chunk, 128-byte swizzle)
-        // at a time; the row sum uses four independent accumulator pairs
         float gsum[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) gsum[u] = 0.f;
-        if (__builtin_expect(!masked, 1)) {
+        Mult8 c8;  // the masked paths' copy of c_g
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float a0 = 0.f, a1 = 0.f;
-            uint32_t w[PV16 ? 8 : 4];
-            float eg[FP4 ? 16 : 1];  // FP4: the group's values, quantised once all are known
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int c = g * 16 + q4 * 4;
-              float x0, x1, x2, x3;
-              fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]),
-                   cg[g], cg[g], bias, bias);
-              fma2(x2, x3, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]),
-                   cg[g], cg[g], bias, bias);
-              const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
-              add2(a0, a1, a0, a1, e0, e1);
-              add2(a0, a1, a0, a1, e2, e3);
-              if constexpr (FP4) {
-                eg[4 * q4] = e0; eg[4 * q4 + 1] = e1; eg[4 * q4 + 2] = e2; eg[4 * q4 + 3] = e3;
-              } else if constexpr (PV16) {
-                w[2 * q4] = pack_p2<true>(e0, e1);
-                w[2 * q4 + 1] = pack_p2<true>(e2, e3);
-              } else {
-                w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
-              }
-            }
-            if constexpr (FP4) fp4_p_group(eg, rho_tab, w);
-            store_p_group<PV16>(my_p, r, g, w);
-            add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
+        for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
+        // the new running max, the rescale factor and the exponent bias; with one P buffer the
+        // buffer is free once P.V of tile j - 1 has completed (with two, P.V of tile j - 2, its
+        // previous reader, completed before this row's rescale wait of tile j - 1 below)
+        auto new_max = [&]() {
+          m_new = fmaxf(m, tile_max);
+          const float m_use = m_new == __int_as_float(0xff800000) ? 0.f : m_new;
+          alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
+          bias = log2_sigma - m_use;
+          if (C::kPBufs == 1 && j > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
+            if (ok) tc_fence_after();
           }
+        };
+        // The unmasked path (every key of the tile visible, causal diagonal and ragged tail
+        // excepted) either runs as one branch from the loads to the last P store (head_dim
+        // 64) or as two branches joined around the max (head_dim 128): measured, each is the
+        // faster arrangement for its head_dim (c4 attention 8.84 vs 8.90 ms; c2 0.1235 vs
+        // 0.1278 ms)
+        if constexpr (DP == 64) {
+          if (__builtin_expect(!masked, 1)) {
+            tile_max = tile_max_regs(tS, sr, cg);
+            trace<TRACE>(p, trs, x, j, 1);
+            trace<TRACE>(p, trs, x, j, 2);
+            new_max();
+            trace<TRACE>(p, trs, x, j, 4);
+            if (ok) tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
+          } else {
+            tile_max = masked_tile_max(tS, limit, c8);
+            trace<TRACE>(p, trs, x, j, 1);
+            trace<TRACE>(p, trs, x, j, 2);
+            new_max();
+            trace<TRACE>(p, trs, x, j, 4);
+            if (ok) gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
+          }
+          if (!ok) break;
         } else {
-          Mult8 c8;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) c8.v[g] = cg[g];
-          gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
+          if (__builtin_expect(!masked, 1)) tile_max = tile_max_regs(tS, sr, cg);
+          else tile_max = masked_tile_max(tS, limit, c8);
+          trace<TRACE>(p, trs, x, j, 1);
+          trace<TRACE>(p, trs, x, j, 2);
+          new_max();
+          if (!ok) break;
+          trace<TRACE>(p, trs, x, j, 4);
+          if (__builtin_expect(!masked, 1)) tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
+          else gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
         // next tile's K scales (used one tile from now): two loads when a K scale group is
@@ -832,8 +867,8 @@ static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3
 cudaError_t launch_attention(const Problem& p, const CUtensorMap* maps, int grid_pairs,
                              cudaStream_t stream) {
   const dim3 grid(p.hq, grid_pairs, p.batch);
-  // the tracing instantiation exists for the E4M3 P·V kernel only
-  if (p.dbg_trace != nullptr && !p.pv16)
+  // the test instantiation (pipeline trace, integer-score dump) exists for the E4M3 P·V kernel
+  if ((p.dbg_trace != nullptr || p.dbg_scores != nullptr) && !p.pv16)
     return p.dp == 64 ? launch_attn_t<64, 0, true>(p, maps, grid, stream)
                       : launch_attn_t<128, 0, true>(p, maps, grid, stream);
   if (p.fp4) return p.dp == 64 ? launch_attn_t<64, 2>(p, maps, grid, stream)

@@ -293,7 +293,10 @@ int sage_debug_select_path(int path);
  * exponentials done, P buffer free, P written, O rescaled; event 7 of the last tile: output
  * written), role 2 = MMA issue (per tile x:
  * 4x+0 P ready, 4x+1 QK^T issued, 4x+2 O ready, 4x+3 P.V issued), role 3 = TMA (K, V
- * issued), for the first 64 KV tiles. NULL turns it off. Process-wide. Returns SAGE_OK. */
+ * issued), for the first 64 KV tiles. NULL turns it off. Process-wide. Returns SAGE_OK.
+ * The events are recorded by a separate test build of the E4M3 P·V attention kernel (the
+ * production build carries no trace points, so its timing differs); calls of the FP16 P·V
+ * and FP4 variants record nothing. */
 int sage_debug_trace_attention(long long* clocks);
 
 /* Converts n floats (device) to FP8 E4M3 (device bytes) with the round-to-nearest-even,

@@ -310,6 +310,14 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   p.batch = batch; p.nq = nq; p.nk = nk; p.varlen = 0; p.vec16 = vec16 ? 1 : 0;
   p.pv16 = pv != 0;  // 1: FP16 P·V variant, 2: FP4 microscaled variant (both on fp16 operands)
   p.fp4 = pv == 2;
+  // Attention CTAs pairs-fastest when the non-causal problem's K / V codes exceed half the 129 MB
+  // L2: the resident CTAs then share one or two heads' K / V instead of re-reading every head's
+  // from DRAM (measured on the 2x48x17776 head_dim 64 shape: 8.795 ms vs 8.839; on 2x8x4096
+  // head_dim 128, whose K / V fit in L2, heads fastest stays faster: 0.1238 vs 0.1252 ms)
+  {
+    const double kv_bytes = (double)batch * hkv * nk * (d <= 64 ? 64 : 128) * 3.0;
+    p.pair_major = (!is_causal && kv_bytes > 64.0 * 1024 * 1024) ? 1 : 0;
+  }
   // element strides (b, h, n) from the layout's dimension order
   auto bhn = [layout](const sage_tensor* t, int64_t& sb, int64_t& sh, int64_t& sn) {
     sb = t->stride[0];

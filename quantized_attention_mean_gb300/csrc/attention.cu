@@ -376,11 +376,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const bool tr = TRACE && p.dbg_trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   // ---- work item: (query head, 256-row pair, sequence); heaviest pairs first when causal
-  const int h = blockIdx.x;
+  // pairs fastest when the host asks for it (non-causal problems whose K / V exceed L2:
+  // consecutive CTAs then share one head's K / V there); otherwise heads fastest, heaviest
+  // pairs first when causal
+  const int lin = (int)blockIdx.x + (int)blockIdx.y * (int)gridDim.x;
+  const int h = p.pair_major ? lin / (int)gridDim.y : (int)blockIdx.x;
   const int b = p.varlen ? p.seqinfo[kSiOrder * p.batch + blockIdx.z] : blockIdx.z;
   const Seq s = get_seq(p, b);
   const int npairs_seq = (s.len_q + 2 * kTileRows - 1) / (2 * kTileRows);
-  const int pair = p.is_causal ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)blockIdx.y;
+  const int pair = p.pair_major ? lin % (int)gridDim.y
+                                : (p.is_causal ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)blockIdx.y);
   if (pair >= npairs_seq || s.len_k <= 0) return;  // uniform across the CTA
   const int q_start = pair * 2 * kTileRows;
   const int rows_a = min(kTileRows, s.len_q - q_start);

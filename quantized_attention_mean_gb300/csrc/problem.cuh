@@ -28,6 +28,7 @@ struct Problem {
   int pv16;                        // P·V on fp16 operands: V^T stored as fp16, P in fp16
   int fp4;                         // FP4 microscaled variant (with pv16): Q, K, V, P carried
                                    // as E2M1 code x E4M3 block scale in fp16
+  int pair_major;                  // attention CTAs ordered pairs-fastest (see api.cu)
   float sm_scale;
   float range_limit;               // smallest float >= 2^38 / N (dense only; varlen per seq)
   const void* q; int64_t q_sb, q_sh, q_sn;

@@ -277,14 +277,19 @@ int sage_attn_debug_scores(const sage_tensor* q, const sage_tensor* k, const sag
  * not for concurrent use. Returns SAGE_OK. */
 int sage_debug_stall_attention(int on);
 
-/* Which implementation dense sage_attn calls use. 0 (default) and 1: the main pipeline
- * (statistics, finalisation, quantisation and the tcgen05 attention kernel: four launches).
- * 2: the short-sequence kernel (pnsm.cn §10: below about 1K tokens fixed costs dominate) for
- * problems with at most 256 keys and 1024 queries, one launch doing the statistics,
- * quantisation and attention per CTA of 128 query rows, with the same arithmetic and results
- * within the same tolerances; other problems, the FP16 P·V variant and calls with the score
- * dump, trace or stall hooks still take the main pipeline. Process-wide; not for concurrent
- * use. Returns SAGE_OK, or SAGE_ERR_INVALID_ARG for another value. */
+/* Which implementation dense sage_attn calls use. The main pipeline is the statistics,
+ * finalisation, quantisation and tcgen05 attention kernels (four launches); the short-sequence
+ * kernel (pnsm.cn §10: below about 1K tokens fixed costs dominate) takes problems with at most
+ * 256 keys and 1024 queries in one launch, doing the statistics, quantisation and attention per
+ * CTA of 128 query rows with the same arithmetic and results within the same tolerances.
+ *   0 (default): the short-sequence kernel for such problems at head_dim <= 64 on a stream that
+ *      is not capturing a CUDA graph, the main pipeline otherwise (measured faster in each
+ *      case: 28 us against 37 per direct call at 256 keys; 22 us against 27 replayed);
+ *   1: always the main pipeline;
+ *   2: the short-sequence kernel whenever the problem fits it.
+ * The FP16 P·V and FP4 variants and calls with the score dump, trace or stall hooks always take
+ * the main pipeline. Process-wide; not for concurrent use. Returns SAGE_OK, or
+ * SAGE_ERR_INVALID_ARG for another value. */
 int sage_debug_select_path(int path);
 
 /* Pipeline trace hook: while `clocks` (device, 4*64*8 int64, caller-owned) is non-NULL, dense

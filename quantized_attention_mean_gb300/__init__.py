@@ -369,9 +369,10 @@ def e4m3(x, stream=None):
 
 
 def select_path(path="auto"):
-    """Which implementation dense calls use: "auto" / "main" (the main pipeline, four launches)
-    or "short" (the one-launch short-sequence kernel for problems with at most 256 keys and
-    1024 queries; larger ones still take the main pipeline). Process-wide."""
+    """Which implementation dense calls use: "auto" (the one-launch short-sequence kernel for
+    head_dim <= 64 problems with at most 256 keys and 1024 queries on a stream that is not
+    capturing a CUDA graph, the four-launch main pipeline otherwise), "main" (always the main
+    pipeline) or "short" (the short-sequence kernel whenever the problem fits it). Process-wide."""
     _check(_lib.load().sage_debug_select_path({"auto": 0, "main": 1, "short": 2}[path]),
            "sage_debug_select_path")
 

@@ -334,15 +334,26 @@ int dense_impl(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
   p.dbg_stall = g_stall;
   p.dbg_trace = g_trace;
   carve(p, L, ws);
-  // The one-launch short-sequence kernel runs when selected and the problem fits (the score
-  // dump, trace and stall hooks belong to the main pipeline's kernels, and the FP16 P·V
-  // variant has no short form). It is not chosen by default: measured, the main pipeline's
-  // four launches replayed from a CUDA graph are faster (256^2 at head_dim 64: 22.5 us per
-  // call against 36.7; direct calls 39.3 against 36.9).
+  // The one-launch short-sequence kernel can take a problem that fits it (the score dump,
+  // trace and stall hooks belong to the main pipeline's kernels, and the FP16 P·V and FP4
+  // variants have no short form). By default it takes the head_dim-64 problems called
+  // directly: measured per call at 256^2, head_dim 64, 28.4 us against 36.8 for the four
+  // launches, and at 1024 x 256 (16 heads) 28.2 against 36.8. Into a CUDA graph being captured
+  // the four launches go instead (replayed they measured 21.7 us against 26.7), and at
+  // head_dim 128 always (52 us against 36 direct, 22 replayed).
   const bool short_ok = pv == 0 && !dbg_scores && !g_trace && !g_stall && nk <= kShortMaxKeys &&
                         nq <= kShortMaxQueries;
-  if (short_ok && g_path == 2) return run_short(p, L, static_cast<cudaStream_t>(stream));
-  return run_pipeline(p, L, nq, nk, static_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (short_ok && g_path == 2) return run_short(p, L, cs);
+  if (short_ok && g_path == 0 && p.dp == 64) {
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusActive;
+    if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) {
+      cudaGetLastError();  // unknown: take the pipeline, which captures either way
+      capture = cudaStreamCaptureStatusActive;
+    }
+    if (capture == cudaStreamCaptureStatusNone) return run_short(p, L, cs);
+  }
+  return run_pipeline(p, L, nq, nk, cs);
 }
 
 }  // namespace

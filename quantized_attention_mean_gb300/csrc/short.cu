@@ -23,10 +23,12 @@
 // The CTAs of one KV head each requantise its K and V (a few hundred KB from L2 at this size);
 // one of them also writes the codes, scales and means into the workspace in the main
 // pipeline's layout, so the quantised state can be read back the same way.
-// Measured (GB300, 256^2 at head_dim 64): 36.7 us per call, against 22.5 us for the main
-// pipeline replayed from a CUDA graph and 39.3 us for its direct calls; the kernel is bound by
-// instruction fetch (each CTA runs its ~10K instructions per warp once, from a cold cache), so
-// it is not the default path.
+// Measured (GB300, 256^2 at head_dim 64): 28.4 us per direct call against 36.8 for the main
+// pipeline's four launches, so it is the default there; replayed from a CUDA graph the four
+// launches are faster (21.7 us against 26.7), and at head_dim 128 they are faster either way,
+// so captured calls and head_dim 128 take the main pipeline. A clock64 trace of one CTA
+// (256 keys, ~46,000 cycles) spends about a third in the attention loop and the rest in the
+// serial statistics and quantisation passes, each latency-bound from a cold instruction cache.
 #include "launch.h"
 #include "problem.cuh"
 #include "sm103_ptx.cuh"
@@ -83,8 +85,8 @@ struct ShortSmem {
   uint8_t* vt8;    // [DP][nks]      V^T E4M3 codes, keys in slot order
   __half* q16;     // [128][DP]      Q codes of the CTA's rows (fp16)
   float *kmean, *vmean, *vscale, *vrcp;   // [DP]
-  unsigned long long *ksum, *vsum;        // [DP]
-  unsigned *vmin, *vmax;                  // [DP] order-preserving codes (min complemented)
+  long long *red_k, *red_v;               // [8 warps][DP] statistics partials, in the V^T / Q
+  float *red_mn, *red_mx;                 // code space (free until the codes are written)
   unsigned *kgmax, *qgmax;                // [nk_pad / 16], [128] group maxima of |x| (float bits)
   float *gscale, *grcp;                   // [nk_pad / 16] K group scale, reciprocal
   float *qscale, *qrcp, *qkt;             // [128] per Q row: its group's scale, reciprocal, LSE term
@@ -92,12 +94,12 @@ struct ShortSmem {
 
 // Byte offsets of the shared-memory arrays for nk_pad keys; returns the total size.
 struct ShortOffsets {
-  size_t rawk, rawv, vt8, q16, kmean, vmean, vscale, vrcp, ksum, vsum, vmin, vmax, gscale, grcp,
+  size_t rawk, rawv, vt8, q16, kmean, vmean, vscale, vrcp, gscale, grcp,
       qscale, qrcp, qkt, kgmax, qgmax, total;
 };
 __host__ __device__ inline ShortOffsets short_offsets(int dp, int nk_pad) {
   ShortOffsets f;
-  const size_t dps = dp + 16, nks = nk_pad + 16;
+  const size_t nks = nk_pad + 16;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o += (bytes + 15) / 16 * 16; return at; };
   f.rawk = take((size_t)nk_pad * dp * 2);
@@ -108,10 +110,6 @@ __host__ __device__ inline ShortOffsets short_offsets(int dp, int nk_pad) {
   f.vmean = take(4 * dp);
   f.vscale = take(4 * dp);
   f.vrcp = take(4 * dp);
-  f.ksum = take(8 * dp);
-  f.vsum = take(8 * dp);
-  f.vmin = take(4 * dp);
-  f.vmax = take(4 * dp);
 
   f.gscale = take(4 * (nk_pad / 16));
   f.grcp = take(4 * (nk_pad / 16));
@@ -139,10 +137,12 @@ __device__ inline ShortSmem short_smem(int dp, int nk_pad, uint8_t* base) {
   L.vmean = reinterpret_cast<float*>(base + f.vmean);
   L.vscale = reinterpret_cast<float*>(base + f.vscale);
   L.vrcp = reinterpret_cast<float*>(base + f.vrcp);
-  L.ksum = reinterpret_cast<unsigned long long*>(base + f.ksum);
-  L.vsum = reinterpret_cast<unsigned long long*>(base + f.vsum);
-  L.vmin = reinterpret_cast<unsigned*>(base + f.vmin);
-  L.vmax = reinterpret_cast<unsigned*>(base + f.vmax);
+  // the statistics partials take 192 dp bytes of the V^T and Q code space (contiguous, at least
+  // dp * (nk_pad + 16 + 256) bytes)
+  L.red_k = reinterpret_cast<long long*>(base + f.vt8);
+  L.red_v = L.red_k + 8 * dp;
+  L.red_mn = reinterpret_cast<float*>(L.red_v + 8 * dp);
+  L.red_mx = L.red_mn + 8 * dp;
   L.kgmax = reinterpret_cast<unsigned*>(base + f.kgmax);
   L.qgmax = reinterpret_cast<unsigned*>(base + f.qgmax);
   L.gscale = reinterpret_cast<float*>(base + f.gscale);
@@ -205,12 +205,6 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     }
   }
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  for (int c = t; c < DP; c += kSThreads) {
-    S.ksum[c] = 0ull;
-    S.vsum[c] = 0ull;
-    S.vmin[c] = 0u;
-    S.vmax[c] = 0u;
-  }
   for (int g = t; g < nk_pad / 16; g += kSThreads) S.kgmax[g] = 0u;
   for (int g = t; g < kSRows; g += kSThreads) S.qgmax[g] = 0u;
   __syncthreads();
@@ -231,6 +225,9 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
       mn[i] = __int_as_float(0x7f800000);
       mx[i] = __int_as_float(0xff800000);
     }
+    // the row loops of the statistics and code passes are unrolled so that independent rows'
+    // shared-memory loads and reductions overlap
+#pragma unroll 4
     for (int n = rg; n < nk; n += RG) {
       float xk[8], xv[8];
       row8(S.rawk, n, xk);
@@ -276,14 +273,27 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
         }
       }
     }
-    if (c0 < d && rg < nk) {
+    // the row groups that share a warp (lanes with the same vec), then the 8 warps through
+    // shared memory (the V^T and Q code space, written only later): shared-memory atomics on
+    // the same 64 or 128 channels from every thread measured 17,000 cycles of this kernel's
+    // 63,000 for 256 keys
+#pragma unroll
+    for (int off = TPR; off < 32; off <<= 1) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (c0 + i >= d) break;
-        atomicAdd(&S.ksum[c0 + i], static_cast<unsigned long long>(ks[i]));
-        atomicAdd(&S.vsum[c0 + i], static_cast<unsigned long long>(vs[i]));
-        atomicMax(&S.vmin[c0 + i], ~ordered_code(mn[i]));
-        atomicMax(&S.vmax[c0 + i], ordered_code(mx[i]));
+        ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], off);
+        vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], off);
+        mn[i] = fminf(mn[i], __shfl_xor_sync(0xffffffffu, mn[i], off));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
+      }
+    }
+    if (lane < TPR) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        S.red_k[warp * DP + c0 + i] = ks[i];
+        S.red_v[warp * DP + c0 + i] = vs[i];
+        S.red_mn[warp * DP + c0 + i] = mn[i];
+        S.red_mx[warp * DP + c0 + i] = mx[i];
       }
     }
   }
@@ -291,10 +301,19 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
   for (int c = t; c < DP; c += kSThreads) {
     float km = 0.f, vm = 0.f, vsc = 0.f, vr = 0.f;
     if (c < d) {
-      km = p.smooth_k ? fixed_point_mean(static_cast<long long>(S.ksum[c]), nk) : 0.f;
-      vm = p.smooth_v ? fixed_point_mean(static_cast<long long>(S.vsum[c]), nk) : 0.f;
-      const float hi = __fsub_rn(ordered_decode(S.vmax[c]), vm);
-      const float lo = __fsub_rn(ordered_decode(~S.vmin[c]), vm);
+      long long ksum = 0, vsum = 0;
+      float vmin = __int_as_float(0x7f800000), vmax = __int_as_float(0xff800000);
+#pragma unroll
+      for (int w = 0; w < kSThreads / 32; ++w) {
+        ksum += S.red_k[w * DP + c];
+        vsum += S.red_v[w * DP + c];
+        vmin = fminf(vmin, S.red_mn[w * DP + c]);
+        vmax = fmaxf(vmax, S.red_mx[w * DP + c]);
+      }
+      km = p.smooth_k ? fixed_point_mean(ksum, nk) : 0.f;
+      vm = p.smooth_v ? fixed_point_mean(vsum, nk) : 0.f;
+      const float hi = __fsub_rn(vmax, vm);
+      const float lo = __fsub_rn(vmin, vm);
       const float a = fmaxf(fabsf(hi), fabsf(lo));
       vsc = a > 0.f ? __fdiv_rn(a, 448.0f) : 0.f;
       vr = a > 0.f ? __fdiv_rn(448.0f, a) : 0.f;
@@ -321,6 +340,7 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     vrcp8[i] = S.vrcp[c0 + i];
   }
   // K: row maxima of |K - mean| (K rows), Q row maxima (registers)
+#pragma unroll 4
   for (int n = rg; n < nk_pad; n += RG) {
     float x[8], a = 0.f;
     if (n < nk) {
@@ -330,8 +350,11 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     }
 #pragma unroll
     for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    // |x| >= 0, so the float bits order like the values
-    if (vec == 0 && n < nk) atomicMax(&S.kgmax[n / p.gk], __float_as_uint(a));
+    // the warp's rows (32 / TPR consecutive keys, within one K group: groups are 16 or 64
+    // keys) to one value; |x| >= 0, so the float bits order like the values
+#pragma unroll
+    for (int off = TPR; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    if (lane == 0 && n < nk) atomicMax(&S.kgmax[n / p.gk], __float_as_uint(a));
   }
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
@@ -341,7 +364,14 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
 #pragma unroll
     for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if (vec == 0) atomicMax(&S.qgmax[(rg + RG * u) / p.gq], __float_as_uint(a));
+    if (p.gq == 1) {
+      if (vec == 0) S.qgmax[rg + RG * u] = __float_as_uint(a);  // one row per group
+    } else {
+      // Q groups of 32 or 128 rows hold the warp's 32 / TPR consecutive rows
+#pragma unroll
+      for (int off = TPR; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+      if (lane == 0) atomicMax(&S.qgmax[(rg + RG * u) / p.gq], __float_as_uint(a));
+    }
   }
   __syncthreads();
   const int gk = p.gk, nkg = (nk + gk - 1) / gk;
@@ -362,6 +392,7 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
   }
   __syncthreads();
   // V codes (rows of V^T in slot order), then K codes into the space of the raw V rows
+#pragma unroll 4
   for (int n = rg; n < nk_pad; n += RG) {
     uint8_t vcode[8];
     if (n < nk) {
@@ -393,6 +424,7 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
       *reinterpret_cast<uint4*>(p.vt + (plane_kv * p.dp + c) * p.vt_pitch + n0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+#pragma unroll 4
   for (int n = rg; n < nk_pad; n += RG) {
     __align__(16) __half kc16[8];
     if (n < nk) {
@@ -478,15 +510,28 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
       mma_f16(sc, qa[ks], b0, b1);
     }
   };
+  // head_dim 64: the tile's scores stay in registers between the max and the exponentials
+  // (64 more registers); head_dim 128 computes them again for the exponentials (its Q
+  // fragments and accumulators leave no room)
+  constexpr bool kKeepScores = DP == 64;
+  float scr[kKeepScores ? kSTile / 8 : 1][4];
   for (int kt = 0; kt * kSTile < kv_end; ++kt) {
     const int key0 = kt * kSTile;
-    // maxima of the scaled scores over this tile's visible keys (the scores are computed again
-    // for the exponentials below: integer MMAs are cheap here, registers are not)
+    // maxima of the scaled scores over this tile's visible keys
     float ta = __int_as_float(0xff800000), tb = ta;
-#pragma unroll 2
+    if constexpr (kKeepScores) {
+#pragma unroll
+      for (int nt = 0; nt < kSTile / 8; ++nt) scores(key0, nt, scr[nt]);
+    }
+#pragma unroll(kKeepScores ? kSTile / 8 : 2)
     for (int nt = 0; nt < kSTile / 8; ++nt) {
       float sc[4];
-      scores(key0, nt, sc);
+      if constexpr (kKeepScores) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = scr[nt % (kSTile / 8)][e];
+      } else {
+        scores(key0, nt, sc);
+      }
       const int j0 = key0 + nt * 8 + 2 * q4;
       const float cj = S.gscale[j0 >> lgk];
       const float ca = sa * cj, cb = sb * cj;
@@ -517,7 +562,7 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     ma = na;
     mb = nb;
     // P~ per 32-key chunk as an A fragment, then P~ V
-#pragma unroll 1
+#pragma unroll(kKeepScores ? kSTile / 32 : 1)
     for (int kc = 0; kc < kSTile / 32; ++kc) {
       uint32_t pa[4];
 #pragma unroll
@@ -527,7 +572,12 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
         for (int u = 0; u < 2; ++u) {
           const int nt = kc * 4 + half * 2 + u;
           float sc[4];
-          scores(key0, nt, sc);
+          if constexpr (kKeepScores) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] = scr[nt % (kSTile / 8)][e];
+          } else {
+            scores(key0, nt, sc);
+          }
           const int j0 = key0 + nt * 8 + 2 * q4;
           const float cj = S.gscale[j0 >> lgk];
           const float ca = sa * cj, cb = sb * cj;

@@ -1,6 +1,8 @@
 """The entry points are capturable into a CUDA graph: no host synchronisation, allocation or
 host-side read of device data inside a call. A graph of several calls (dense, FP16 P·V and
-varlen), replayed, gives the same bytes as the direct calls and leaves the status clear."""
+varlen), replayed, gives the same bytes as the direct calls and leaves the status clear; the
+default path choice for short problems (short-sequence kernel when called directly, the main
+pipeline when captured) is checked against each implementation selected explicitly."""
 
 import pytest
 import torch
@@ -84,3 +86,45 @@ def test_varlen_graph_replay_matches_direct_call():
     assert qa.read_device_status(ws) == 0
     assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), ref_l.view(torch.int32))
+
+
+def test_auto_path_direct_short_captured_main():
+    # a short head_dim-64 problem: called directly the default path runs the short-sequence
+    # kernel (same bytes as selecting it), captured into a graph it runs the main pipeline
+    # (same bytes as selecting that)
+    import quantized_attention_mean_gb300 as qa
+    dev = torch.device("cuda:0")
+    w = Workload("auto_path", 1, 4, 2, 300, 200, 64, dtype="bf16", gran="per_warp", accum="fp32",
+                 return_lse=True, smooth_v=True)
+    q, k, v = (t.to(dev) for t in dense_inputs(w, 4))
+    ws = qa.alloc_workspace(qa.workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran), dev)
+    out, lse = torch.empty_like(q), torch.empty(w.B, w.Hq, w.Nq, device=dev)
+    res = {}
+    try:
+        for path in ("main", "short", "auto"):
+            qa.select_path(path)
+            _dense_call(qa, w, q, k, v, out, lse, ws, False)
+            torch.cuda.synchronize()
+            res[path] = (out.clone(), lse.clone())
+        qa.select_path("auto")
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            _dense_call(qa, w, q, k, v, out, lse, ws, False)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            _dense_call(qa, w, q, k, v, out, lse, ws, False)
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+    finally:
+        qa.select_path("auto")
+    assert qa.read_device_status(ws) == 0
+    same = lambda a, b: (torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+                         and torch.equal(a[1].view(torch.int32), b[1].view(torch.int32)))
+    assert same(res["auto"], res["short"])
+    assert same((out, lse), res["main"])
+    assert not same(res["main"], res["short"])  # the two implementations round differently

@@ -213,7 +213,25 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
   };
 
   // ---- 1. statistics: exact fixed-point sums of K and V, V's min / max per channel (the
-  // sums as biased 32-bit split words, as the statistics kernel forms them)
+  // sums as biased 32-bit split words, as the statistics kernel forms them); and the Q group
+  // maxima (Q needs no statistics)
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    float x[8], a = 0.f;
+    unpack8<T>(qraw[u], x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
+#pragma unroll
+    for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    if (p.gq == 1) {
+      if (vec == 0) S.qgmax[rg + RG * u] = __float_as_uint(a);  // one row per group
+    } else {
+      // Q groups of 32 or 128 rows hold the warp's 32 / TPR consecutive rows
+#pragma unroll
+      for (int off = TPR; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+      if (lane == 0) atomicMax(&S.qgmax[(rg + RG * u) / p.gq], __float_as_uint(a));
+    }
+  }
   {
     unsigned kh[8], kl[8], vh[8], vl[8];
     float mn[8], mx[8], amax = 0.f;
@@ -339,15 +357,30 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     vmean8[i] = S.vmean[c0 + i];
     vrcp8[i] = S.vrcp[c0 + i];
   }
-  // K: row maxima of |K - mean| (K rows), Q row maxima (registers)
+  // one pass over the key rows: the row maxima of |K - mean| and the V codes (rows of V^T in
+  // slot order)
 #pragma unroll 4
   for (int n = rg; n < nk_pad; n += RG) {
     float x[8], a = 0.f;
+    uint8_t vcode[8];
     if (n < nk) {
       row8(S.rawk, n, x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) a = fmaxf(a, c0 + i < d ? fabsf(__fsub_rn(x[i], kmean8[i])) : 0.f);
+      float xv[8];
+      row8(S.rawv, n, xv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float vsm = c0 + i < d ? __fsub_rn(xv[i], vmean8[i]) : 0.f;
+        vcode[i] = static_cast<uint8_t>(pack_e4m3x2(__fmul_rn(vsm, vrcp8[i]), 0.f) & 0xffu);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vcode[i] = 0;
     }
+    const int sl = v_slot(n);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S.vt8[(c0 + i) * S.nks + sl] = vcode[i];
 #pragma unroll
     for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     // the warp's rows (32 / TPR consecutive keys, within one K group: groups are 16 or 64
@@ -355,23 +388,6 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
 #pragma unroll
     for (int off = TPR; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     if (lane == 0 && n < nk) atomicMax(&S.kgmax[n / p.gk], __float_as_uint(a));
-  }
-#pragma unroll
-  for (int u = 0; u < QPT; ++u) {
-    float x[8], a = 0.f;
-    unpack8<T>(qraw[u], x);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
-#pragma unroll
-    for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if (p.gq == 1) {
-      if (vec == 0) S.qgmax[rg + RG * u] = __float_as_uint(a);  // one row per group
-    } else {
-      // Q groups of 32 or 128 rows hold the warp's 32 / TPR consecutive rows
-#pragma unroll
-      for (int off = TPR; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-      if (lane == 0) atomicMax(&S.qgmax[(rg + RG * u) / p.gq], __float_as_uint(a));
-    }
   }
   __syncthreads();
   const int gk = p.gk, nkg = (nk + gk - 1) / gk;
@@ -391,27 +407,7 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
     if (rr == g0 && r0 + rr < nq) p.sq[plane_q * p.sq_pp + (r0 + rr) / gq] = sc;
   }
   __syncthreads();
-  // V codes (rows of V^T in slot order), then K codes into the space of the raw V rows
-#pragma unroll 4
-  for (int n = rg; n < nk_pad; n += RG) {
-    uint8_t vcode[8];
-    if (n < nk) {
-      float xv[8];
-      row8(S.rawv, n, xv);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float vsm = c0 + i < d ? __fsub_rn(xv[i], vmean8[i]) : 0.f;
-        vcode[i] = static_cast<uint8_t>(pack_e4m3x2(__fmul_rn(vsm, vrcp8[i]), 0.f) & 0xffu);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) vcode[i] = 0;
-    }
-    const int sl = v_slot(n);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) S.vt8[(c0 + i) * S.nks + sl] = vcode[i];
-  }
-  __syncthreads();
+  // then the K codes, into the space of the raw V rows (the V codes are all written)
   if (kv_writer) {
     // V^T codes to the workspace in natural key order, 16 keys (one 16-byte store) at a time
     const int nchunk = (nk + 15) / 16;

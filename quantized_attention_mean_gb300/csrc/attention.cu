@@ -18,7 +18,11 @@
 //               shared memory, rescales its O row in tensor memory when the max grows, and
 //               finally writes O = acc . s_v / l + v_mean and the LSE.
 // The two tiles ping-pong: while one tile's softmax runs, the tensor core computes the other
-// tile's scores. Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// tile's scores. Tensor memory at head_dim 128: S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512). At head_dim 64 three S buffers [0,384) rotate over the tiles in issue order
+// (A_0, B_0, A_1, B_1, ...; item n in buffer n % 3), O_A [384,448), O_B [448,512): as soon as a
+// tile's softmax has published its P, the scores three items ahead go into its buffer, so each
+// tile's next S is computed while its current softmax still runs.
 //
 // Variants (template argument PV): 0 = E4M3 P and V on kind::f8f6f4; 1 = the FP16 P·V
 // variant (P and V' in fp16 on kind::f16); 2 = the FP4 microscaled variant (pwwt.cn guide
@@ -55,12 +59,19 @@ struct AttnCfg {
   // P buffers per query tile: with two, the softmax writes P_j while P.V of tile j - 1 may
   // still be reading P_{j-1} (the FP16 P·V variant has room for one)
   static constexpr int kPBufs = PV16 ? 1 : 2;
+  // S buffers in tensor memory: at head_dim 64 three 128-column buffers serve the two query
+  // tiles in rotation (item n = tile j of query tile x, n = j * tiles + x, uses buffer n % 3),
+  // so a tile's next scores are computed while its softmax still runs; at 128 the two O
+  // accumulators leave room for one buffer per query tile
+  static constexpr int kSBufs = DP == 64 ? 3 : 2;
+  static constexpr uint32_t kTmemO = kSBufs * 128;  // O of query tile x at kTmemO + x * DP
+  static_assert(kTmemO + 2 * DP <= 512, "tensor memory columns");
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBufs * kPTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 2;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + kSBufs + 6 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRho = kOffMisc + 64;  // FP4: fl32(6 / s) per E4M3 code s (128)
   static constexpr int kBytes = kOffRho + 128 * 4;
@@ -363,8 +374,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;
   uint64_t* v_empty = v_full + C::kVStages;
-  uint64_t* s_full = v_empty + C::kVStages;  // [2]
-  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* s_full = v_empty + C::kVStages;  // [kSBufs]
+  uint64_t* p_full = s_full + C::kSBufs;     // [2]
   uint64_t* o_full = p_full + 2;             // [2]
   uint64_t* o_ready = o_full + 2;            // [2]
   uint64_t* drain = o_ready + 2;             // [2]
@@ -403,8 +414,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+    for (int i = 0; i < C::kSBufs; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_ready[i], 128);
@@ -495,7 +506,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // The whole warp runs the issue loop converged and one elected lane issues each MMA and
     // commit (warp-uniform operands). Both query tiles' MMAs are issued alternating A and B,
     // so the two tiles' softmax phases stay offset by half an iteration and the tensor core
-    // serves one while the other computes.
+    // serves one while the other computes. With one S buffer per tile (head_dim 128) a tile's
+    // next QK^T waits for its own P; with three in rotation (head_dim 64) it is issued when
+    // the other tile publishes its previous P, about half an iteration earlier.
     {
       const bool tr_mma = tr && lane == 0;
       const int nx = has_b ? 2 : 1;
@@ -508,8 +521,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto wait_all = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
       };
-      auto issue_qk = [&](int x, int st) {
-        const uint32_t d_s = tmem + (x ? 128u : 0u);
+      // S of query tile x into S buffer sb from K stage st
+      auto issue_qk = [&](int x, int sb, int st) {
+        const uint32_t d_s = tmem + static_cast<uint32_t>(sb) * 128u;
         const uint64_t qx = dq + static_cast<uint64_t>((x * C::kQTileBytes) >> 4);
         const uint64_t kst = dk + static_cast<uint64_t>((st * C::kKTileBytes) >> 4);
 #pragma unroll
@@ -517,10 +531,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t off = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
           mma_f16_ss_warp(d_s, qx + off, kst + off, idesc_qk(), k > 0);
         }
-        mma_commit_warp(&s_full[x]);
+        mma_commit_warp(&s_full[sb]);
       };
       auto issue_pv = [&](int x, int sv, int buf, bool first) {
-        const uint32_t d_o = tmem + (x ? 384u : 256u);
+        const uint32_t d_o = tmem + C::kTmemO + static_cast<uint32_t>(x * DP);
         const uint64_t px =
             dp + static_cast<uint64_t>(((x * C::kPBufs + buf) * C::kPTileBytes) >> 4);
         const uint64_t vst = dv + static_cast<uint64_t>((sv * C::kVTileBytes) >> 4);
@@ -539,10 +553,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit_warp(&o_full[x]);
       };
-      bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+      bool ok = wait_all(q_full, 0);
+      if constexpr (C::kSBufs == 3) {
+        // Items n = j * nx + x in order. Once the softmax of item n has published P (its S
+        // buffer is free and, for j > 0, its O rows are rescaled), the scores of item n + 3 go
+        // into that buffer (the other query tile's next tile when both exist, which its softmax
+        // needs only after its current tile), then P_j(x) V_j.
+        const int n_items = n_tiles * nx;
+        auto qk_item = [&](int n) {
+          const int kj = n / nx, xx = n - kj * nx, st = kj % C::kKStages;
+          if (xx == 0) {
+            if (!wait_all(&k_full[st], (kj / C::kKStages) & 1)) return false;
+            tc_fence_after();
+          }
+          issue_qk(xx, n % 3, st);
+          if (xx == nx - 1) mma_commit_warp(&k_empty[st]);
+          return true;
+        };
+        for (int n = 0; n < 3 && n < n_items && ok; ++n) ok = qk_item(n);
+        for (int n = 0; n < n_items && ok; ++n) {
+          const int j = n / nx, x = n - j * nx, sv = j % C::kVStages;
+          ok = wait_all(&p_full[x], j & 1);
+          if (!ok) break;
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
+          tc_fence_after();
+          if (n + 3 < n_items) ok = qk_item(n + 3);
+          if (!ok) break;
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
+          if (x == 0) {
+            ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
+          issue_pv(x, sv, j % C::kPBufs, j == 0);
+          if (x == nx - 1) mma_commit_warp(&v_empty[sv]);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
+        }
+      } else {
+      if (ok) ok = wait_all(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < nx; ++x) issue_qk(x, 0);
+        for (int x = 0; x < nx; ++x) issue_qk(x, x, 0);
         mma_commit_warp(&k_empty[0]);
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
@@ -558,7 +610,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (x == 0) ok = wait_all(&k_full[nst], ((j + 1) / C::kKStages) & 1);
             if (!ok) break;
             tc_fence_after();
-            issue_qk(x, nst);
+            issue_qk(x, x, nst);
           }
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
           // O(x) rescaled for the new running max: accumulate P_j(x) V_j
@@ -575,6 +627,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j + 1 < n_tiles) mma_commit_warp(&k_empty[nst]);
         mma_commit_warp(&v_empty[sv]);
       }
+      }
       // every MMA must have finished before tensor memory is released
       mma_commit_warp(&drain[0]);
       volatile int never = 0;
@@ -589,8 +642,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int x = warp >> 2;               // tile A or B
     const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + (x == 0 ? 0u : 128u);
-    const uint32_t tO = tmem + lane_base + (x == 0 ? 256u : 384u);
+    constexpr bool kRing = C::kSBufs == 3;  // S buffers in rotation (head_dim 64)
+    const int nx = has_b ? 2 : 1;
+    const uint32_t tO = tmem + lane_base + C::kTmemO + static_cast<uint32_t>(x * DP);
+    // this query tile's S buffer (head_dim 128; at 64 the buffer rotates per tile)
+    uint32_t tS = tmem + lane_base + (x == 0 ? 0u : 128u);
     uint8_t* const p_row = sP + x * C::kPBufs * C::kPTileBytes + r * 128;  // + buffer offset
     const int xrows = x == 0 ? rows_a : rows_b;
     const bool active_tile = x == 0 || has_b;
@@ -617,7 +673,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int row_limit = p.is_causal ? min(s.len_k, i + 1) : s.len_k;
     if (active_tile) {
       for (int j = 0; j < n_tiles; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
+        if constexpr (kRing) {
+          const int n_item = j * nx + x;
+          tS = tmem + lane_base + static_cast<uint32_t>(n_item % 3) * 128u;
+          ok = __all_sync(0xffffffffu, mbar_wait(&s_full[n_item % 3], (n_item / 3) & 1, abort_flag));
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
+        }
         if (!ok) break;
         trace<TRACE>(p, trs, x, j, 0);
         tc_fence_after();
@@ -709,13 +771,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         trace<TRACE>(p, trs, x, j, 3);
         l = l * alpha + rs;
         m = m_new;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&p_full[x]);
-        trace<TRACE>(p, trs, x, j, 5);
-        // rescale this warp's O rows for the grown max while the next scores are computed;
-        // P_j(x) V_j is issued only after o_ready. O holds the sum up to tile j - 1 once P.V
-        // of tile j - 1 is complete.
+        if constexpr (!kRing) {
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&p_full[x]);
+          trace<TRACE>(p, trs, x, j, 5);
+        }
+        // rescale this warp's O rows for the grown max: O holds the sum up to tile j - 1 once
+        // P.V of tile j - 1 is complete. With one S buffer per query tile this runs while the
+        // tile's next scores are computed and P_j(x) V_j waits for o_ready; with the S buffers
+        // in rotation the next scores are already there, and P_j(x) is published after it
+        // (the wait for P.V of tile j - 1 also keeps p_full one phase ahead of the MMA issuer
+        // at most).
         if (C::kPBufs > 1 && j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
           if (!ok) break;
@@ -743,8 +810,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           tmem_wait_st();
         }
-        tc_fence_before();
-        mbar_arrive(&o_ready[x]);
+        if constexpr (kRing) {
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&p_full[x]);
+          trace<TRACE>(p, trs, x, j, 5);
+        } else {
+          tc_fence_before();
+          mbar_arrive(&o_ready[x]);
+        }
         trace<TRACE>(p, trs, x, j, 6);
       }
       // ---- epilogue: out = acc . s_v / l + v_mean, then the LSE. The output address, the LSE

@@ -54,8 +54,8 @@ struct AttnCfg {
   static constexpr int kKTileBytes = kTileKeys * DP * 2;
   static constexpr int kVTileBytes = DP * kTileKeys * (PV16 ? 2 : 1);    // V^T, E4M3 or fp16
   static constexpr int kPTileBytes = kTileRows * kTileKeys * (PV16 ? 2 : 1);  // E4M3 or fp16
-  static constexpr int kKStages = DP == 128 ? 2 : 3;
-  static constexpr int kVStages = DP == 128 ? (PV16 ? 1 : 2) : 3;
+  static constexpr int kKStages = DP == 128 ? 2 : 4;
+  static constexpr int kVStages = DP == 128 ? (PV16 ? 1 : 2) : 4;
   // P buffers per query tile: with two, the softmax writes P_j while P.V of tile j - 1 may
   // still be reading P_{j-1} (the FP16 P·V variant has room for one)
   static constexpr int kPBufs = PV16 ? 1 : 2;
@@ -65,6 +65,9 @@ struct AttnCfg {
   // accumulators leave room for one buffer per query tile
   static constexpr int kSBufs = DP == 64 ? 3 : 2;
   static constexpr uint32_t kTmemO = kSBufs * 128;  // O of query tile x at kTmemO + x * DP
+  // with the rotating S buffers a K tile is needed a tile ahead of its V tile anyway: K and V
+  // of one tile share a stage, one full barrier (k_full) and one release (k_empty)
+  static constexpr bool kKVShared = kSBufs == 3;
   static_assert(kTmemO + 2 * DP <= 512, "tensor memory columns");
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
@@ -78,6 +81,10 @@ struct AttnCfg {
   // one CTA per SM (the kernel allocates all 512 tensor-memory columns)
   static constexpr int kSmem = (kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024);
   static_assert(kBytes + 1024 <= 232448, "shared memory budget");
+  // shared stages: the MMA issuer asks for K_{j+3} (the scores three items ahead, one query
+  // tile) before it issues P_j V_j, whose completion releases the stage of tile j + 3 - stages;
+  // so a single query tile needs more than three stages
+  static_assert(!kKVShared || (kKStages == kVStages && kKStages >= 4), "shared K / V stages");
 };
 
 // Instruction descriptors: M = 128 rows, fp32 accumulate, K-major operands.
@@ -470,23 +477,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j >= C::kKStages) ok = mbar_wait(&k_empty[st], ((j / C::kKStages) - 1) & 1, abort_flag);
         if (!ok) break;
         trace<TRACE>(p, tr, 3, j, 0);
-        mbar_arrive_expect_tx(&k_full[st], C::kKTileBytes);
+        mbar_arrive_expect_tx(&k_full[st], C::kKTileBytes + (C::kKVShared ? C::kVTileBytes : 0));
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sK + st * C::kKTileBytes + c * kTileKeys * 128, &tmK, &k_full[st], c * 64,
                       krow, (int)plane_kv);
         ++issued_k;
         const int sv = j % C::kVStages;
-        if (j >= C::kVStages) ok = mbar_wait(&v_empty[sv], ((j / C::kVStages) - 1) & 1, abort_flag);
-        if (!ok) break;
+        uint64_t* const vbar = C::kKVShared ? &k_full[st] : &v_full[sv];
+        if constexpr (!C::kKVShared) {
+          if (j >= C::kVStages) ok = mbar_wait(&v_empty[sv], ((j / C::kVStages) - 1) & 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
+        }
         trace<TRACE>(p, tr, 3, j, 1);
-        mbar_arrive_expect_tx(&v_full[sv], C::kVTileBytes);
         if constexpr (PV16) {
           // fp16 V^T: two 64-key chunks of DP rows x 128 bytes
           for (int c = 0; c < 2; ++c)
-            tma_load_3d(sV + sv * C::kVTileBytes + c * DP * 128, &tmV, &v_full[sv], krow + c * 64, 0,
+            tma_load_3d(sV + sv * C::kVTileBytes + c * DP * 128, &tmV, vbar, krow + c * 64, 0,
                         (int)plane_kv);
         } else {
-          tma_load_3d(sV + sv * C::kVTileBytes, &tmV, &v_full[sv], krow, 0, (int)plane_kv);
+          tma_load_3d(sV + sv * C::kVTileBytes, &tmV, vbar, krow, 0, (int)plane_kv);
         }
         ++issued_v;
       }
@@ -496,8 +506,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_wait(q_full, 0, &never);
         for (int j = max(0, issued_k - C::kKStages); j < issued_k; ++j)
           mbar_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1, &never);
-        for (int j = max(0, issued_v - C::kVStages); j < issued_v; ++j)
-          mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, &never);
+        if (!C::kKVShared)
+          for (int j = max(0, issued_v - C::kVStages); j < issued_v; ++j)
+            mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, &never);
         record_error(p.err, kDevTimeout);
       }
     }
@@ -567,7 +578,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
           }
           issue_qk(xx, n % 3, st);
-          if (xx == nx - 1) mma_commit_warp(&k_empty[st]);
           return true;
         };
         for (int n = 0; n < 3 && n < n_items && ok; ++n) ok = qk_item(n);
@@ -580,14 +590,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (n + 3 < n_items) ok = qk_item(n + 3);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
-          if (x == 0) {
-            ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
-            if (!ok) break;
-            tc_fence_after();
-          }
+          // (V_j arrived with K_j, waited for before the first QK^T of tile j)
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
           issue_pv(x, sv, j % C::kPBufs, j == 0);
-          if (x == nx - 1) mma_commit_warp(&v_empty[sv]);
+          if (x == nx - 1) mma_commit_warp(&k_empty[sv]);  // K_j and V_j released together
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
         }
       } else {

@@ -50,6 +50,7 @@ CASES = [
     Workload("pad_d40_nhd", 1, 2, 2, 160, 200, 40, layout="NHD", gran="per_block", smooth_v=True,
              v_offset_std=1.0),
     Workload("short_keys", 1, 2, 2, 129, 1, 64, gran="per_warp", smooth_v=True),
+    Workload("one_tile_long_keys", 1, 2, 2, 100, 1000, 64, gran="per_warp", return_lse=True),
 ]
 
 _cache = {}

@@ -49,6 +49,13 @@ CASES = [
              accum="fp32", return_lse=True, k_offset_std=2.0),
     Workload("pad_d40_nhd", 1, 2, 2, 160, 200, 40, layout="NHD", gran="per_block", smooth_v=True,
              v_offset_std=1.0),
+    # CTAs with one query tile (Nq <= 128, and the last 256-row pair of Nq = 300) walking more
+    # key tiles than the pipeline holds in flight: at head_dim 64 the issuer then runs three
+    # S buffers ahead of the single tile's softmax through every K / V stage
+    Workload("one_tile_long_keys", 1, 2, 2, 100, 1000, 64, gran="per_warp", return_lse=True),
+    Workload("tail_pair_long_keys", 1, 2, 2, 300, 1100, 64, dtype="bf16", gran="per_thread",
+             smooth_v=True, v_offset_std=1.0),
+    Workload("one_tile_long_keys_d128", 1, 2, 2, 100, 700, 128, gran="per_warp", return_lse=True),
 ]
 
 

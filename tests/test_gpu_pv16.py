@@ -24,6 +24,8 @@ CASES = [
              smooth_v=True, k_offset_std=4.0, v_offset_std=2.0, return_lse=True),
     Workload("fp16acc_d128", 1, 2, 2, 512, 512, 128, gran="per_warp", accum="fp16+fp32"),
     Workload("pad_d72", 1, 2, 1, 140, 260, 72, dtype="bf16", gran="per_thread", accum="fp32+fp32"),
+    Workload("tail_pair_long_keys", 1, 2, 2, 300, 1100, 64, dtype="bf16", gran="per_thread",
+             smooth_v=True, v_offset_std=1.0),
 ]
 
 

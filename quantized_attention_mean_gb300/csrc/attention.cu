@@ -6,8 +6,8 @@
 // KV tiles of 128 keys:
 //   warp 8      TMA producer: Q tiles once, then K tiles (integer-valued fp16 codes) and
 //               V^T tiles (E4M3) through a ring of shared-memory stages;
-//   warp 9      allocates tensor memory and issues the MMAs from one thread (A and B
-//               alternating):
+//   warp 9      allocates tensor memory and issues the MMAs from one elected thread (A and
+//               B alternating; at head_dim 64 warp 10 issues tile B's, see below):
 //               S = Q8 . K8^T  (tcgen05 kind::f16 on the INT8 codes: every product and partial
 //                               sum is an integer below 2^24, so the fp32 accumulator holds
 //                               the exact INT32 score),
@@ -22,7 +22,10 @@
 // O_B [384,512). At head_dim 64 three S buffers [0,384) rotate over the tiles in issue order
 // (A_0, B_0, A_1, B_1, ...; item n in buffer n % 3), O_A [384,448), O_B [448,512): as soon as a
 // tile's softmax has published its P, the scores three items ahead go into its buffer, so each
-// tile's next S is computed while its current softmax still runs.
+// tile's next S is computed while its current softmax still runs. There each query tile has
+// its own MMA issuer (warp 9 for A, warp 10 for B): an issuer waits on its tile's P, issues
+// the scores three items ahead and then its tile's P.V, so one issuer's barrier waits and
+// commits overlap the other's MMAs.
 //
 // Variants (template argument PV): 0 = E4M3 P and V on kind::f8f6f4; 1 = the FP16 P·V
 // variant (P and V' in fp16 on kind::f16); 2 = the FP4 microscaled variant (pwwt.cn guide
@@ -39,7 +42,8 @@
 namespace sage {
 
 // 12 warps = 3 warpgroups: softmax A (warps 0-3), softmax B (4-7), and a control warpgroup
-// (warp 8 TMA, warp 9 MMA + TMEM allocation, warps 10-11 idle). Launched at 168 registers
+// (warp 8 TMA, warp 9 MMA + TMEM allocation, warp 10 tile B's MMA at head_dim 64, warp 11
+// idle). Launched at 168 registers
 // per thread (the per-sub-partition limit with 3 warps each); the control warpgroup drops to
 // 56 and the softmax warpgroups rise to 224: 2*128*224 + 128*56 = 12*32*168.
 constexpr int kAttnThreads = 384;
@@ -419,7 +423,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // ---- set-up: barriers, tensor memory
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+    // shared K / V stages are released by each query tile's MMA issuer
+    const int k_rel = C::kKVShared && has_b ? 2 : 1;
+    for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], k_rel); }
     for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
     for (int i = 0; i < C::kSBufs; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         record_error(p.err, kDevTimeout);
       }
     }
-   } else if (warp == 9) {
+   } else if (warp == 9 || (C::kSBufs == 3 && warp == 10 && has_b)) {
     // =========================================================== MMA issuer
     // The whole warp runs the issue loop converged and one elected lane issues each MMA and
     // commit (warp-uniform operands). Both query tiles' MMAs are issued alternating A and B,
@@ -523,6 +529,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     {
       const bool tr_mma = tr && lane == 0;
       const int nx = has_b ? 2 : 1;
+      const int me = warp - 9;  // with rotating S buffers: the issuer of query tile me's items
       // descriptor bases; a K step inside a 128-byte row adds its byte offset / 16 to the
       // start-address field (no carry: shared-memory addresses stay below 2^18)
       const uint64_t dq = sdesc_sw128(smem_u32(sQ));
@@ -571,18 +578,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // into that buffer (the other query tile's next tile when both exist, which its softmax
         // needs only after its current tile), then P_j(x) V_j.
         const int n_items = n_tiles * nx;
+        // QK^T of item n into S buffer n % 3 (after this issuer's own wait for K_kj: the
+        // other issuer's wait orders nothing for this thread)
         auto qk_item = [&](int n) {
           const int kj = n / nx, xx = n - kj * nx, st = kj % C::kKStages;
-          if (xx == 0) {
-            if (!wait_all(&k_full[st], (kj / C::kKStages) & 1)) return false;
-            tc_fence_after();
-          }
+          if (!wait_all(&k_full[st], (kj / C::kKStages) & 1)) return false;
+          tc_fence_after();
           issue_qk(xx, n % 3, st);
           return true;
         };
-        for (int n = 0; n < 3 && n < n_items && ok; ++n) ok = qk_item(n);
-        for (int n = 0; n < n_items && ok; ++n) {
-          const int j = n / nx, x = n - j * nx, sv = j % C::kVStages;
+        if (me == 0) {
+          for (int n = 0; n < 3 && n < n_items && ok; ++n) ok = qk_item(n);
+        } else {
+          // the stages of tiles 0 and 1 are first read by this issuer's P.V
+          for (int kj = 0; kj < 2 && kj < n_tiles && ok; ++kj) {
+            ok = wait_all(&k_full[kj], 0);
+            if (ok) tc_fence_after();
+          }
+        }
+        // each issuer walks its own query tile's items; the scores of item n + 3 (the other
+        // tile's, when both exist) are issued by the issuer of item n
+        for (int n = me; n < n_items && ok; n += nx) {
+          const int j = n / nx, x = me, sv = j % C::kVStages;
           ok = wait_all(&p_full[x], j & 1);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
@@ -590,10 +607,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (n + 3 < n_items) ok = qk_item(n + 3);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
-          // (V_j arrived with K_j, waited for before the first QK^T of tile j)
+          // (V_j arrived with K_j, which this issuer waited for at an earlier item)
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
           issue_pv(x, sv, j % C::kPBufs, j == 0);
-          if (x == nx - 1) mma_commit_warp(&k_empty[sv]);  // K_j and V_j released together
+          mma_commit_warp(&k_empty[sv]);  // this issuer's last use of K_j and V_j
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
         }
       } else {
@@ -635,9 +652,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       }
       // every MMA must have finished before tensor memory is released
-      mma_commit_warp(&drain[0]);
+      mma_commit_warp(&drain[me]);
       volatile int never = 0;
-      mbar_wait(&drain[0], 0, &never);
+      mbar_wait(&drain[me], 0, &never);
       __syncwarp();
       if (!ok && lane == 0) record_error(p.err, kDevTimeout);
     }

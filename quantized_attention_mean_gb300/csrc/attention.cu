@@ -604,13 +604,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
           tc_fence_after();
-          if (n + 3 < n_items) ok = qk_item(n + 3);
+          // one P buffer per tile: the softmax waits for P_j(x) V_j before its next
+          // exponentials, so that product goes first; otherwise the other tile's scores do
+          if (C::kPBufs > 1 && n + 3 < n_items) ok = qk_item(n + 3);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
           // (V_j arrived with K_j, which this issuer waited for at an earlier item)
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
           issue_pv(x, sv, j % C::kPBufs, j == 0);
           mma_commit_warp(&k_empty[sv]);  // this issuer's last use of K_j and V_j
+          if (C::kPBufs == 1 && n + 3 < n_items) ok = qk_item(n + 3);
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
         }
       } else {

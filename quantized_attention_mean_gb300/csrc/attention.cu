@@ -24,7 +24,7 @@
 // tile's softmax has published its P, the scores three items ahead go into its buffer, so each
 // tile's next S is computed while its current softmax still runs. There each query tile has
 // its own MMA issuer (warp 9 for A, warp 10 for B): an issuer waits on its tile's P, issues
-// the scores three items ahead and then its tile's P.V, so one issuer's barrier waits and
+// its tile's P.V and then the scores three items ahead, so one issuer's barrier waits and
 // commits overlap the other's MMAs.
 //
 // Variants (template argument PV): 0 = E4M3 P and V on kind::f8f6f4; 1 = the FP16 P·V
@@ -574,9 +574,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = wait_all(q_full, 0);
       if constexpr (C::kSBufs == 3) {
         // Items n = j * nx + x in order. Once the softmax of item n has published P (its S
-        // buffer is free and, for j > 0, its O rows are rescaled), the scores of item n + 3 go
-        // into that buffer (the other query tile's next tile when both exist, which its softmax
-        // needs only after its current tile), then P_j(x) V_j.
+        // buffer is free and, for j > 0, its O rows are rescaled), P_j(x) V_j is issued and
+        // the scores of item n + 3 go into that buffer (the other query tile's next tile when
+        // both exist, which its softmax needs only after its current tile).
         const int n_items = n_tiles * nx;
         // QK^T of item n into S buffer n % 3 (after this issuer's own wait for K_kj: the
         // other issuer's wait orders nothing for this thread)
@@ -604,16 +604,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
           tc_fence_after();
-          // one P buffer per tile: the softmax waits for P_j(x) V_j before its next
-          // exponentials, so that product goes first; otherwise the other tile's scores do
-          if (C::kPBufs > 1 && n + 3 < n_items) ok = qk_item(n + 3);
-          if (!ok) break;
-          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
+          // P_j(x) V_j first (the softmax waits for it before publishing its next P, or with
+          // one P buffer before its next exponentials), then the scores three items ahead
           // (V_j arrived with K_j, which this issuer waited for at an earlier item)
-          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
           issue_pv(x, sv, j % C::kPBufs, j == 0);
           mma_commit_warp(&k_empty[sv]);  // this issuer's last use of K_j and V_j
-          if (C::kPBufs == 1 && n + 3 < n_items) ok = qk_item(n + 3);
+          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
+          if (n + 3 < n_items) ok = qk_item(n + 3);
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
         }
       } else {

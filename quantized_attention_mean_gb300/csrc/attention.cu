@@ -6,8 +6,8 @@
 // KV tiles of 128 keys:
 //   warp 8      TMA producer: Q tiles once, then K tiles (integer-valued fp16 codes) and
 //               V^T tiles (E4M3) through a ring of shared-memory stages;
-//   warp 9      allocates tensor memory and issues the MMAs from one elected thread (A and
-//               B alternating; at head_dim 64 warp 10 issues tile B's, see below):
+//   warps 9, 10 issue the MMAs from one elected thread each, warp 9 for query tile A (and
+//               allocates tensor memory), warp 10 for tile B:
 //               S = Q8 . K8^T  (tcgen05 kind::f16 on the INT8 codes: every product and partial
 //                               sum is an integer below 2^24, so the fp32 accumulator holds
 //                               the exact INT32 score),
@@ -18,14 +18,14 @@
 //               shared memory, rescales its O row in tensor memory when the max grows, and
 //               finally writes O = acc . s_v / l + v_mean and the LSE.
 // The two tiles ping-pong: while one tile's softmax runs, the tensor core computes the other
-// tile's scores. Tensor memory at head_dim 128: S_A [0,128), S_B [128,256), O_A [256,384),
-// O_B [384,512). At head_dim 64 three S buffers [0,384) rotate over the tiles in issue order
-// (A_0, B_0, A_1, B_1, ...; item n in buffer n % 3), O_A [384,448), O_B [448,512): as soon as a
-// tile's softmax has published its P, the scores three items ahead go into its buffer, so each
-// tile's next S is computed while its current softmax still runs. There each query tile has
-// its own MMA issuer (warp 9 for A, warp 10 for B): an issuer waits on its tile's P, issues
-// its tile's P.V and then the scores three items ahead, so one issuer's barrier waits and
-// commits overlap the other's MMAs.
+// tile's scores, and each tile's next S is computed while its current softmax still runs.
+// Tensor memory at head_dim 128: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); a
+// tile's issuer starts its next QK^T as soon as the softmax holds S in registers (s_free),
+// and its P.V once P is written and O rescaled (o_ready). At head_dim 64 three S buffers
+// [0,384) rotate over the tiles in issue order (A_0, B_0, A_1, B_1, ...; item n in buffer
+// n % 3), O_A [384,448), O_B [448,512): once a tile's softmax has published P (p_full), its
+// issuer issues the tile's P.V and then the scores three items ahead into the freed buffer.
+// With one issuer per tile, one issuer's barrier waits and commits overlap the other's MMAs.
 //
 // Variants (template argument PV): 0 = E4M3 P and V on kind::f8f6f4; 1 = the FP16 P·V
 // variant (P and V' in fp16 on kind::f16); 2 = the FP4 microscaled variant (pwwt.cn guide
@@ -42,7 +42,7 @@
 namespace sage {
 
 // 12 warps = 3 warpgroups: softmax A (warps 0-3), softmax B (4-7), and a control warpgroup
-// (warp 8 TMA, warp 9 MMA + TMEM allocation, warp 10 tile B's MMA at head_dim 64, warp 11
+// (warp 8 TMA, warp 9 tile A's MMAs + TMEM allocation, warp 10 tile B's MMAs, warp 11
 // idle). Launched at 168 registers
 // per thread (the per-sub-partition limit with 3 warps each); the control warpgroup drops to
 // 56 and the softmax warpgroups rise to 224: 2*128*224 + 128*56 = 12*32*168.
@@ -78,7 +78,7 @@ struct AttnCfg {
   static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kVTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBufs * kPTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + kSBufs + 6 + 2;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + kSBufs + 6 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRho = kOffMisc + 64;  // FP4: fl32(6 / s) per E4M3 code s (128)
   static constexpr int kBytes = kOffRho + 128 * 4;
@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* o_full = p_full + 2;             // [2]
   uint64_t* o_ready = o_full + 2;            // [2]
   uint64_t* drain = o_ready + 2;             // [2]
+  uint64_t* s_free = drain + 2;              // [2] (one S buffer per tile: S read into registers)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   float* rho_tab = reinterpret_cast<float*>(sm + C::kOffRho);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
@@ -424,9 +425,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     // shared K / V stages are released by each query tile's MMA issuer
-    const int k_rel = C::kKVShared && has_b ? 2 : 1;
+    const int k_rel = has_b ? 2 : 1;
     for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], k_rel); }
-    for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+    for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], k_rel); }
     for (int i = 0; i < C::kSBufs; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 128);
@@ -435,6 +436,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    mbar_init(&s_free[0], 128);
+    mbar_init(&s_free[1], 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -518,18 +521,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         record_error(p.err, kDevTimeout);
       }
     }
-   } else if (warp == 9 || (C::kSBufs == 3 && warp == 10 && has_b)) {
+   } else if (warp == 9 || (warp == 10 && has_b)) {
     // =========================================================== MMA issuer
     // The whole warp runs the issue loop converged and one elected lane issues each MMA and
-    // commit (warp-uniform operands). Both query tiles' MMAs are issued alternating A and B,
-    // so the two tiles' softmax phases stay offset by half an iteration and the tensor core
-    // serves one while the other computes. With one S buffer per tile (head_dim 128) a tile's
-    // next QK^T waits for its own P; with three in rotation (head_dim 64) it is issued when
-    // the other tile publishes its previous P, about half an iteration earlier.
+    // commit (warp-uniform operands). Each query tile has its own issuer; a stage of K / V is
+    // released by one commit from each issuer that read it.
     {
       const bool tr_mma = tr && lane == 0;
       const int nx = has_b ? 2 : 1;
-      const int me = warp - 9;  // with rotating S buffers: the issuer of query tile me's items
+      const int me = warp - 9;  // this issuer's query tile
       // descriptor bases; a K step inside a 128-byte row adds its byte offset / 16 to the
       // start-address field (no carry: shared-memory addresses stay below 2^18)
       const uint64_t dq = sdesc_sw128(smem_u32(sQ));
@@ -618,38 +618,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok) ok = wait_all(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < nx; ++x) issue_qk(x, x, 0);
+        issue_qk(me, me, 0);
         mma_commit_warp(&k_empty[0]);
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int sv = j % C::kVStages;
         const int nst = (j + 1) % C::kKStages;
-        for (int x = 0; x < nx && ok; ++x) {
-          // S_j(x) consumed and P_j(x) written: the tile's next scores can start right away
-          ok = wait_all(&p_full[x], j & 1);
+        const int x = me;
+        if (j + 1 < n_tiles) {
+          // S_j(x) is in the softmax's registers: the tile's next scores can start
+          ok = wait_all(&s_free[x], j & 1);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);
-          tc_fence_after();
-          if (j + 1 < n_tiles) {
-            if (x == 0) ok = wait_all(&k_full[nst], ((j + 1) / C::kKStages) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(x, x, nst);
-          }
-          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
-          // O(x) rescaled for the new running max: accumulate P_j(x) V_j
-          ok = wait_all(&o_ready[x], j & 1);
-          if (!ok) break;
-          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
-          if (x == 0) ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
+          ok = wait_all(&k_full[nst], ((j + 1) / C::kKStages) & 1);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(x, sv, j % C::kPBufs, j == 0);
-          trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
+          issue_qk(x, x, nst);
+          mma_commit_warp(&k_empty[nst]);
         }
+        trace<TRACE>(p, tr_mma, 2, j, 4 * x + 1);
+        // P_j(x) written and O(x) rescaled for the new running max: accumulate P_j(x) V_j
+        ok = wait_all(&o_ready[x], j & 1);
         if (!ok) break;
-        if (j + 1 < n_tiles) mma_commit_warp(&k_empty[nst]);
+        trace<TRACE>(p, tr_mma, 2, j, 4 * x + 2);
+        ok = wait_all(&v_full[sv], (j / C::kVStages) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(x, sv, j % C::kPBufs, j == 0);
         mma_commit_warp(&v_empty[sv]);
+        trace<TRACE>(p, tr_mma, 2, j, 4 * x + 3);
       }
       }
       // every MMA must have finished before tensor memory is released
@@ -766,15 +763,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           if (!ok) break;
         } else {
-          if (__builtin_expect(!masked, 1)) tile_max = tile_max_regs(tS, sr, cg);
-          else tile_max = masked_tile_max(tS, limit, c8);
+          if (__builtin_expect(!masked, 1)) {
+            tile_max = tile_max_regs(tS, sr, cg);
+            tc_fence_before();
+            mbar_arrive(&s_free[x]);
+          } else {
+            tile_max = masked_tile_max(tS, limit, c8);
+          }
           trace<TRACE>(p, trs, x, j, 1);
           trace<TRACE>(p, trs, x, j, 2);
           new_max();
           if (!ok) break;
           trace<TRACE>(p, trs, x, j, 4);
-          if (__builtin_expect(!masked, 1)) tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
-          else gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
+          if (__builtin_expect(!masked, 1)) {
+            tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
+          } else {
+            gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
+            tc_fence_before();
+            mbar_arrive(&s_free[x]);
+          }
         }
         const float rs = ((gsum[0] + gsum[1]) + (gsum[2] + gsum[3])) + ((gsum[4] + gsum[5]) + (gsum[6] + gsum[7]));
         // next tile's K scales (used one tile from now): two loads when a K scale group is
@@ -795,12 +802,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         trace<TRACE>(p, trs, x, j, 3);
         l = l * alpha + rs;
         m = m_new;
-        if constexpr (!kRing) {
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(&p_full[x]);
-          trace<TRACE>(p, trs, x, j, 5);
-        }
+        trace<TRACE>(p, trs, x, j, 5);
         // rescale this warp's O rows for the grown max: O holds the sum up to tile j - 1 once
         // P.V of tile j - 1 is complete. With one S buffer per query tile this runs while the
         // tile's next scores are computed and P_j(x) V_j waits for o_ready; with the S buffers
@@ -840,6 +842,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_arrive(&p_full[x]);
           trace<TRACE>(p, trs, x, j, 5);
         } else {
+          // P_j(x) and the rescaled O together
+          fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&o_ready[x]);
         }

@@ -268,7 +268,9 @@ int run_short(Problem& p, const Layout& L, cudaStream_t st) {
   auto mark = [&](int i) { if (ev) cudaEventRecord(ev->e[i], st); };
   cudaError_t e;
   mark(0);
-  if ((e = cudaMemsetAsync(p.err, 0, L.off_ksum - L.off_err, st)) != cudaSuccess)
+  // a one-thread clear kernel rather than a memset, so that the short kernel (launched as a
+  // programmatic dependent) starts while it finishes
+  if ((e = launch_short_status_clear(p.err, static_cast<int>((L.off_ksum - L.off_err) / 4), st)) != cudaSuccess)
     return cuda_fail(e, "status reset");
   mark(1);
   mark(2);

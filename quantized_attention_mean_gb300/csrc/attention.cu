@@ -804,11 +804,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m = m_new;
         trace<TRACE>(p, trs, x, j, 5);
         // rescale this warp's O rows for the grown max: O holds the sum up to tile j - 1 once
-        // P.V of tile j - 1 is complete. With one S buffer per query tile this runs while the
-        // tile's next scores are computed and P_j(x) V_j waits for o_ready; with the S buffers
-        // in rotation the next scores are already there, and P_j(x) is published after it
-        // (the wait for P.V of tile j - 1 also keeps p_full one phase ahead of the MMA issuer
-        // at most).
+        // P.V of tile j - 1 is complete. P_j(x) V_j is issued only after the rescale: with one
+        // S buffer per tile (head_dim 128) o_ready carries P_j and the rescaled O together; with
+        // the S buffers in rotation P_j(x) is published after it, and the wait for P.V of tile
+        // j - 1 also keeps p_full at most one phase ahead of the MMA issuer.
         if (C::kPBufs > 1 && j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], (j - 1) & 1, abort_flag));
           if (!ok) break;

@@ -29,6 +29,7 @@ int note_cuda_failure(cudaError_t e, const char* where);
 
 cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st);
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st);
+cudaError_t launch_short_status_clear(int* err, int words, cudaStream_t st);
 cudaError_t launch_finalize(const Problem& p, int n_stats, cudaStream_t st);
 cudaError_t launch_quant(const Problem& p, int max_len_q, int max_len_k, cudaStream_t st);
 cudaError_t launch_export_codes(const __half* codes, int64_t rows_pp, int dp, int d, int planes,

@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   for (int g = t; g < nk_pad / 16; g += kSThreads) S.kgmax[g] = 0u;
   for (int g = t; g < kSRows; g += kSThreads) S.qgmax[g] = 0u;
+  // the status word is cleared by the launch before this one (which may still be finishing):
+  // nothing in the workspace is touched before it has
+  pdl_wait();
   __syncthreads();
   auto row8 = [&](const uint8_t* raw, int n, float (&x)[8]) {
     unpack8<T>(*reinterpret_cast<const uint4*>(raw + ((size_t)n * DP + c0) * 2), x);
@@ -632,6 +635,12 @@ __global__ void __launch_bounds__(kSThreads, 1) short_attn_kernel(const Problem 
   }
 }
 
+// Clears the call's status words; lets the short kernel's launch start at once.
+__global__ void short_status_clear(int* err, int n) {
+  pdl_trigger();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) err[i] = 0;
+}
+
 template <typename T, int DP>
 cudaError_t launch_short_t(const Problem& p, cudaStream_t st) {
   const int nk_pad = (p.nk + kSTile - 1) / kSTile * kSTile;
@@ -640,11 +649,16 @@ cudaError_t launch_short_t(const Problem& p, cudaStream_t st) {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.nq + kSRows - 1) / kSRows, p.hq, p.batch);
-  short_attn_kernel<T, DP><<<grid, kSThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t el = launch_pdl(short_attn_kernel<T, DP>, grid, dim3(kSThreads), smem, st, p);
+  return el != cudaSuccess ? el : cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_short_status_clear(int* err, int words, cudaStream_t st) {
+  short_status_clear<<<1, 32, 0, st>>>(err, words);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_short_attention(const Problem& p, cudaStream_t st) {
   if (p.dtype == 0)

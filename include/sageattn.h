@@ -28,7 +28,9 @@
  *   - The workspace must be 256-byte aligned, at least sage_attn_workspace_size() bytes,
  *     and must not be shared by calls that may run concurrently.
  *   - Thread safety: calls from several host threads are safe; the only global state is a
- *     per-device cache of the kernels' shared-memory opt-in.
+ *     per-device cache of the kernels' shared-memory opt-in (and of whether the device is
+ *     supported). A cudaDeviceReset clears the opt-in but not the cache: do not reset a
+ *     device the library has already launched on.
  */
 #ifndef SAGEATTN_H
 #define SAGEATTN_H

@@ -964,7 +964,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int DP, int PV, bool TRACE = false>
 static cudaError_t launch_attn_t(const Problem& p, const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
   constexpr int smem = AttnCfg<DP, PV != 0>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<DP, PV, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<int> limits[64];
+  cudaError_t e = raise_smem_limit(attn_kernel<DP, PV, TRACE>, smem, limits);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<DP, PV, TRACE>, grid, dim3(kAttnThreads), smem, stream, maps[0],
                     maps[1], maps[2], p);

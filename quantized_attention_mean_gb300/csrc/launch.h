@@ -1,5 +1,6 @@
 // Host-side launchers of the kernels (defined next to each kernel).
 #pragma once
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "problem.cuh"
@@ -21,6 +22,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device,
+// calling the runtime only when the limit recorded for that device is lower (the same kernel is
+// launched on every call). `limits` is one per kernel: the largest value set on each device.
+template <typename K>
+cudaError_t raise_smem_limit(K* kernel, int bytes, std::atomic<int> (&limits)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  }
+  if (limits[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) {
+    int cur = limits[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !limits[dev].compare_exchange_weak(cur, bytes)) {
+    }
+  }
+  return e;
 }
 
 // Records a failed CUDA call for sage_last_cuda_error (calling thread) and returns

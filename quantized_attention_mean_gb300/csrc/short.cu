@@ -645,8 +645,8 @@ template <typename T, int DP>
 cudaError_t launch_short_t(const Problem& p, cudaStream_t st) {
   const int nk_pad = (p.nk + kSTile - 1) / kSTile * kSTile;
   const size_t smem = short_offsets(DP, nk_pad).total;
-  const cudaError_t e = cudaFuncSetAttribute(short_attn_kernel<T, DP>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<int> limits[64];
+  const cudaError_t e = raise_smem_limit(short_attn_kernel<T, DP>, (int)smem, limits);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.nq + kSRows - 1) / kSRows, p.hq, p.batch);
   const cudaError_t el = launch_pdl(short_attn_kernel<T, DP>, grid, dim3(kSThreads), smem, st, p);

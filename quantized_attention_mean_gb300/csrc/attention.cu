@@ -327,29 +327,76 @@ __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const
   }
 }
 
-// Max over a fully visible tile of S * c_g, the scores loaded into registers sr.
+// 16 consecutive 32-bit TMEM columns into r[OFF .. OFF + 16) (thread t: lane (lane field of
+// taddr) + t), and their maximum as fp32 into m: the reducing form of the load. Both are valid
+// only after a tcgen05.wait::ld (tmem_wait_ld for r, tmem_wait_ld_max for m).
+template <int OFF>
+__device__ __forceinline__ void tmem_ld16_max(uint32_t taddr, uint32_t (&r)[32], float& m) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+      : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]),
+        "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]),
+        "=r"(r[OFF + 10]), "=r"(r[OFF + 11]), "=r"(r[OFF + 12]), "=r"(r[OFF + 13]),
+        "=r"(r[OFF + 14]), "=r"(r[OFF + 15]), "=f"(m)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_max(float (&m)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(m[0]), "+f"(m[1]), "+f"(m[2]), "+f"(m[3]), "+f"(m[4]), "+f"(m[5]), "+f"(m[6]),
+                 "+f"(m[7])
+               :
+               : "memory");
+}
+
+// Max over a fully visible tile of S * c_g, the scores loaded into registers sr (c_g >= 0
+// keeps the order). At head_dim 64 each 16-key group's largest raw integer score comes with its
+// load (the reducing form of tcgen05.ld); at 128, where that form measured slower (the extra
+// live values spill), the raw scores are maximised with three-input max instructions.
+template <int DP>
 __device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32], const float (&cg)[8]) {
-  tmem_ld32(tS + 0, sr[0]);
-  tmem_ld32(tS + 32, sr[1]);
-  tmem_ld32(tS + 64, sr[2]);
-  tmem_ld32(tS + 96, sr[3]);
-  tmem_wait_ld(sr[0]);
-  tmem_wait_ld(sr[1]);
-  tmem_wait_ld(sr[2]);
-  tmem_wait_ld(sr[3]);
-  // max of the raw integer scores per sub-group (three-input max), then scaled (c_g >= 0
-  // keeps the order)
-  float tile_max = __int_as_float(0xff800000);
+  if constexpr (DP == 64) {
+    float gm[8];
+    tmem_ld16_max<0>(tS + 0, sr[0], gm[0]);
+    tmem_ld16_max<16>(tS + 16, sr[0], gm[1]);
+    tmem_ld16_max<0>(tS + 32, sr[1], gm[2]);
+    tmem_ld16_max<16>(tS + 48, sr[1], gm[3]);
+    tmem_ld16_max<0>(tS + 64, sr[2], gm[4]);
+    tmem_ld16_max<16>(tS + 80, sr[2], gm[5]);
+    tmem_ld16_max<0>(tS + 96, sr[3], gm[6]);
+    tmem_ld16_max<16>(tS + 112, sr[3], gm[7]);
+    tmem_wait_ld(sr[0]);
+    tmem_wait_ld(sr[1]);
+    tmem_wait_ld(sr[2]);
+    tmem_wait_ld(sr[3]);
+    tmem_wait_ld_max(gm);
+    float tile_max = __int_as_float(0xff800000);
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
-    float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-    for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-    a = fmaxf(a, __uint_as_float(v[15]));
-    tile_max = fmaxf(tile_max, a * cg[g]);
+    for (int g = 0; g < 8; ++g) tile_max = fmaxf(tile_max, gm[g] * cg[g]);
+    return tile_max;
+  } else {    tmem_ld32(tS + 0, sr[0]);
+    tmem_ld32(tS + 32, sr[1]);
+    tmem_ld32(tS + 64, sr[2]);
+    tmem_ld32(tS + 96, sr[3]);
+    tmem_wait_ld(sr[0]);
+    tmem_wait_ld(sr[1]);
+    tmem_wait_ld(sr[2]);
+    tmem_wait_ld(sr[3]);
+    // max of the raw integer scores per sub-group (three-input max), then scaled (c_g >= 0
+    // keeps the order)
+    float tile_max = __int_as_float(0xff800000);
+  #pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
+      float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+  #pragma unroll
+      for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+      a = fmaxf(a, __uint_as_float(v[15]));
+      tile_max = fmaxf(tile_max, a * cg[g]);
+    }
+    return tile_max;
   }
-  return tile_max;
 }
 
 // Records clock64() for (role, tile, event) when tracing is on and this is CTA (0,0,0). Only
@@ -747,7 +794,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // 0.1278 ms)
         if constexpr (DP == 64) {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs(tS, sr, cg);
+            tile_max = tile_max_regs<DP>(tS, sr, cg);
             trace<TRACE>(p, trs, x, j, 1);
             trace<TRACE>(p, trs, x, j, 2);
             new_max();
@@ -764,7 +811,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
         } else {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs(tS, sr, cg);
+            tile_max = tile_max_regs<DP>(tS, sr, cg);
             tc_fence_before();
             mbar_arrive(&s_free[x]);
           } else {

@@ -330,6 +330,22 @@ __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const
 // 16 consecutive 32-bit TMEM columns into r[OFF .. OFF + 16) (thread t: lane (lane field of
 // taddr) + t), and their maximum as fp32 into m: the reducing form of the load. Both are valid
 // only after a tcgen05.wait::ld (tmem_wait_ld for r, tmem_wait_ld_max for m).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& m) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_max4(float (&m)[4]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(m[0]), "+f"(m[1]), "+f"(m[2]), "+f"(m[3]) : : "memory");
+}
 template <int OFF>
 __device__ __forceinline__ void tmem_ld16_max(uint32_t taddr, uint32_t (&r)[32], float& m) {
   asm volatile(
@@ -351,12 +367,27 @@ __device__ __forceinline__ void tmem_wait_ld_max(float (&m)[8]) {
 }
 
 // Max over a fully visible tile of S * c_g, the scores loaded into registers sr (c_g >= 0
-// keeps the order). At head_dim 64 each 16-key group's largest raw integer score comes with its
-// load (the reducing form of tcgen05.ld); at 128, where that form measured slower (the extra
-// live values spill), the raw scores are maximised with three-input max instructions.
+// keeps the order). The largest raw integer score of each K scale group's columns comes with
+// their load (the reducing form of tcgen05.ld): per 32 columns at head_dim 128 with 64-key K
+// groups, per 16 columns otherwise (the 16-column form at head_dim 128 with 64-key groups
+// measured slower than the 32-column one).
 template <int DP>
-__device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32], const float (&cg)[8]) {
-  if constexpr (DP == 64) {
+__device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32], const float (&cg)[8],
+                                              int lgk) {
+  if (DP == 128 && lgk == 6) {
+    float cm[4];
+    tmem_ld32_max(tS + 0, sr[0], cm[0]);
+    tmem_ld32_max(tS + 32, sr[1], cm[1]);
+    tmem_ld32_max(tS + 64, sr[2], cm[2]);
+    tmem_ld32_max(tS + 96, sr[3], cm[3]);
+    tmem_wait_ld(sr[0]);
+    tmem_wait_ld(sr[1]);
+    tmem_wait_ld(sr[2]);
+    tmem_wait_ld(sr[3]);
+    tmem_wait_ld_max4(cm);
+    return fmaxf(fmaxf(cm[0] * cg[0], cm[1] * cg[2]), fmaxf(cm[2] * cg[4], cm[3] * cg[6]));
+  }
+  {
     float gm[8];
     tmem_ld16_max<0>(tS + 0, sr[0], gm[0]);
     tmem_ld16_max<16>(tS + 16, sr[0], gm[1]);
@@ -374,27 +405,6 @@ __device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32
     float tile_max = __int_as_float(0xff800000);
 #pragma unroll
     for (int g = 0; g < 8; ++g) tile_max = fmaxf(tile_max, gm[g] * cg[g]);
-    return tile_max;
-  } else {    tmem_ld32(tS + 0, sr[0]);
-    tmem_ld32(tS + 32, sr[1]);
-    tmem_ld32(tS + 64, sr[2]);
-    tmem_ld32(tS + 96, sr[3]);
-    tmem_wait_ld(sr[0]);
-    tmem_wait_ld(sr[1]);
-    tmem_wait_ld(sr[2]);
-    tmem_wait_ld(sr[3]);
-    // max of the raw integer scores per sub-group (three-input max), then scaled (c_g >= 0
-    // keeps the order)
-    float tile_max = __int_as_float(0xff800000);
-  #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint32_t* v = &sr[g >> 1][(g & 1) * 16];
-      float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-  #pragma unroll
-      for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-      a = fmaxf(a, __uint_as_float(v[15]));
-      tile_max = fmaxf(tile_max, a * cg[g]);
-    }
     return tile_max;
   }
 }
@@ -794,7 +804,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // 0.1278 ms)
         if constexpr (DP == 64) {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs<DP>(tS, sr, cg);
+            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk);
             trace<TRACE>(p, trs, x, j, 1);
             trace<TRACE>(p, trs, x, j, 2);
             new_max();
@@ -811,7 +821,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
         } else {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs<DP>(tS, sr, cg);
+            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk);
             tc_fence_before();
             mbar_arrive(&s_free[x]);
           } else {

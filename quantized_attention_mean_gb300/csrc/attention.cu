@@ -210,6 +210,18 @@ __device__ __forceinline__ uint32_t pack_p2(float lo, float hi) {
   }
 }
 
+// Four values as E4M3 bytes of one word, the first in the lowest byte (RNE, saturating).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(w)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return w;
+}
+
 // Largest of 16 values.
 __device__ __forceinline__ float max16(const float (&e)[16]) {
   float m = max3(e[0], e[1], e[2]);
@@ -291,7 +303,7 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
 // P~ = fmt(2^(S * c_g + bias)) of every key of a fully visible tile whose scores sr are in
 // registers, written to the row's P buffer; the unquantised values are summed into gsum (four
 // independent accumulator pairs).
-template <int PV>
+template <int PV, int DP>
 __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const float (&cg)[8],
                                               float bias, uint8_t* my_p, int r,
                                               const float* rho_tab, float (&gsum)[8]) {
@@ -317,7 +329,10 @@ __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const
       } else if constexpr (PV16) {
         w[2 * q4] = pack_p2<true>(e0, e1);
         w[2 * q4 + 1] = pack_p2<true>(e2, e3);
+      } else if constexpr (DP == 64) {
+        w[q4] = pack_e4m3x4(e0, e1, e2, e3);
       } else {
+        // (the four-value pack measured slower at head_dim 128: c2 0.1206 vs 0.1175 ms)
         w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
       }
     }
@@ -809,7 +824,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             trace<TRACE>(p, trs, x, j, 2);
             new_max();
             trace<TRACE>(p, trs, x, j, 4);
-            if (ok) tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
+            if (ok) tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum);
           } else {
             tile_max = masked_tile_max(tS, limit, c8);
             trace<TRACE>(p, trs, x, j, 1);
@@ -833,7 +848,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
           trace<TRACE>(p, trs, x, j, 4);
           if (__builtin_expect(!masked, 1)) {
-            tile_exp_regs<PV>(sr, cg, bias, my_p, r, rho_tab, gsum);
+            tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum);
           } else {
             gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
             tc_fence_before();

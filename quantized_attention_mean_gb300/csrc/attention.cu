@@ -337,7 +337,15 @@ __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const
       }
     }
     if constexpr (FP4) fp4_p_group(eg, rho_tab, w);
-    store_p_group<PV16>(my_p, r, g, w);
+    if constexpr (!PV16 && DP == 64) {
+      // (the same swizzled 16-byte unit as store_p_group, addressed in the shared window:
+      // measured faster at head_dim 64)
+      const uint32_t a = smem_u32(my_p) + static_cast<uint32_t>((g ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                   "r"(w[3]) : "memory");
+    } else {
+      store_p_group<PV16>(my_p, r, g, w);
+    }
     add2(gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], gsum[2 * (g & 3)], gsum[2 * (g & 3) + 1], a0, a1);
   }
 }

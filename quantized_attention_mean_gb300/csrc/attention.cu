@@ -772,12 +772,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int g = 0; g < 8; ++g) skn[g] = g * 16 < s.len_k ? __ldg(&skp[(g * 16) >> lgk]) : 0.f;
     // keys this row may see: [0, row_limit) (causal: j <= i; always: j < len_k)
     const int row_limit = p.is_causal ? min(s.len_k, i + 1) : s.len_k;
+    // S buffer (item n = j * nx + x mod 3) and its phase parity ((n / 3) mod 2), advanced by nx
+    // items per tile
+    int s_buf = x, s_par = 0;
     if (active_tile) {
       for (int j = 0; j < n_tiles; ++j) {
         if constexpr (kRing) {
-          const int n_item = j * nx + x;
-          tS = tmem + lane_base + static_cast<uint32_t>(n_item % 3) * 128u;
-          ok = __all_sync(0xffffffffu, mbar_wait(&s_full[n_item % 3], (n_item / 3) & 1, abort_flag));
+          tS = tmem + lane_base + static_cast<uint32_t>(s_buf) * 128u;
+          ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s_buf], s_par, abort_flag));
+          s_buf += nx;
+          if (s_buf >= 3) {
+            s_buf -= 3;
+            s_par ^= 1;
+          }
         } else {
           ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag));
         }

@@ -658,10 +658,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // the scores of item n + 3 go into that buffer (the other query tile's next tile when
         // both exist, which its softmax needs only after its current tile).
         const int n_items = n_tiles * nx;
+        const int lnx = nx - 1;  // log2(nx): items n = j * nx + x
         // QK^T of item n into S buffer n % 3 (after this issuer's own wait for K_kj: the
         // other issuer's wait orders nothing for this thread)
         auto qk_item = [&](int n) {
-          const int kj = n / nx, xx = n - kj * nx, st = kj % C::kKStages;
+          const int kj = n >> lnx, xx = n & lnx, st = kj % C::kKStages;
           if (!wait_all(&k_full[st], (kj / C::kKStages) & 1)) return false;
           tc_fence_after();
           issue_qk(xx, n % 3, st);
@@ -679,7 +680,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // each issuer walks its own query tile's items; the scores of item n + 3 (the other
         // tile's, when both exist) are issued by the issuer of item n
         for (int n = me; n < n_items && ok; n += nx) {
-          const int j = n / nx, x = me, sv = j % C::kVStages;
+          const int j = n >> lnx, x = me, sv = j % C::kVStages;
           ok = wait_all(&p_full[x], j & 1);
           if (!ok) break;
           trace<TRACE>(p, tr_mma, 2, j, 4 * x + 0);

@@ -103,6 +103,39 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Four MMAs of one kind into d from one elected lane of a converged warp: operands (a_k, b_k),
+// k = 0..3, the first accumulating when acc0 != 0 and the others always.
+template <bool F8>
+__device__ __forceinline__ void mma4_warp(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                          uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3,
+                                          uint32_t idesc, uint32_t acc0) {
+  if constexpr (F8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %10, %10;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, q;\n\t}" ::"r"(d),
+        "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(acc0)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %10, %10;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, q;\n\t}" ::"r"(d),
+        "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(acc0)
+        : "memory");
+  }
+}
+
 // a[idx] for a runtime idx in [0, 32) without indexing a register array.
 __device__ __forceinline__ uint32_t pick32(const uint32_t (&a)[32], int idx) {
   uint32_t v = a[0];
@@ -624,10 +657,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t d_s = tmem + static_cast<uint32_t>(sb) * 128u;
         const uint64_t qx = dq + static_cast<uint64_t>((x * C::kQTileBytes) >> 4);
         const uint64_t kst = dk + static_cast<uint64_t>((st * C::kKTileBytes) >> 4);
+        // K = head_dim in steps of 16 (32 bytes) inside 64-channel chunks of 128-byte rows; at
+        // head_dim 64 the four MMAs from one elected block (measured faster there, not at 128)
+        if constexpr (DP == 64) {
+          mma4_warp<false>(d_s, qx, qx + 2, qx + 4, qx + 6, kst, kst + 2, kst + 4, kst + 6, idesc_qk(), 0u);
+        } else {
 #pragma unroll
-        for (int k = 0; k < DP / 16; ++k) {
-          const uint32_t off = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
-          mma_f16_ss_warp(d_s, qx + off, kst + off, idesc_qk(), k > 0);
+          for (int k = 0; k < DP / 16; ++k) {
+            const uint32_t off = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
+            mma_f16_ss_warp(d_s, qx + off, kst + off, idesc_qk(), k > 0);
+          }
         }
         mma_commit_warp(&s_full[sb]);
       };
@@ -638,16 +677,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t vst = dv + static_cast<uint64_t>((sv * C::kVTileBytes) >> 4);
         if constexpr (PV16) {
           // K = 128 keys in steps of 16 (32 bytes) inside 64-key chunks
+          if constexpr (DP == 64) {
 #pragma unroll
-          for (int k = 0; k < kTileKeys / 16; ++k) {
-            const uint32_t op = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
-            const uint32_t ov = ((k >> 2) * (DP * 128) + (k & 3) * 32) >> 4;
-            mma_f16_ss_warp(d_o, px + op, vst + ov, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t op = (c * (kTileRows * 128)) >> 4;
+              const uint32_t ov = (c * (DP * 128)) >> 4;
+              mma4_warp<false>(d_o, px + op, px + op + 2, px + op + 4, px + op + 6, vst + ov, vst + ov + 2,
+                               vst + ov + 4, vst + ov + 6, idesc_pv<DP>(), (!first || c > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kTileKeys / 16; ++k) {
+              const uint32_t op = ((k >> 2) * (kTileRows * 128) + (k & 3) * 32) >> 4;
+              const uint32_t ov = ((k >> 2) * (DP * 128) + (k & 3) * 32) >> 4;
+              mma_f16_ss_warp(d_o, px + op, vst + ov, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+            }
           }
         } else {
+          if constexpr (DP == 64) {
+            mma4_warp<true>(d_o, px, px + 2, px + 4, px + 6, vst, vst + 2, vst + 4, vst + 6, idesc_pv<DP>(),
+                            first ? 0u : 1u);
+          } else {
 #pragma unroll
-          for (int k = 0; k < kTileKeys / 32; ++k)
-            mma_f8_ss_warp(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kTileKeys / 32; ++k)
+              mma_f8_ss_warp(d_o, px + 2 * k, vst + 2 * k, idesc_pv<DP>(), (!first || k > 0) ? 1u : 0u);
+          }
         }
         mma_commit_warp(&o_full[x]);
       };

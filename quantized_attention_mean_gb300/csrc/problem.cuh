@@ -10,7 +10,7 @@ namespace sage {
 
 constexpr int kTileRows = 128;   // query rows per attention tile, tokens per quantisation tile
 constexpr int kTileKeys = 128;   // keys per attention KV tile
-// tokens per block in the K/V statistics pass (4 rows per thread, dp/8 threads per row)
+// tokens per batch of the K/V statistics pass (4 rows per thread, dp/8 threads per row)
 __host__ __device__ constexpr int stats_chunk(int dp) { return 8192 / dp; }
 
 // Device-side status codes (mirror sage_status in include/sageattn.h).

@@ -11,8 +11,47 @@
 // __float2int_rn) so no contraction or reassociation can change a code.
 #include "launch.h"
 #include "problem.cuh"
+#include "sm103_ptx.cuh"
 
 namespace sage {
+
+// Two 16-bit floats of one input word as fp32 (low half first), exactly.
+template <typename T> __device__ __forceinline__ void unpack2(uint32_t w, float& a, float& b);
+template <> __device__ __forceinline__ void unpack2<__nv_bfloat16>(uint32_t w, float& a, float& b) {
+  a = __uint_as_float(w << 16);
+  b = __uint_as_float(w & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ void unpack2<__half>(uint32_t w, float& a, float& b) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+  a = f.x;
+  b = f.y;
+}
+// Lane-wise min / max / larger magnitude of two raw fp16 or bf16 pairs (exact; a NaN lane
+// yields the other operand, as fminf / fmaxf do; the magnitude form's sign bits are not used).
+template <typename T> __device__ __forceinline__ uint32_t hmin2_raw(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (std::is_same<T, __half>::value) asm("min.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <typename T> __device__ __forceinline__ uint32_t hmax2_raw(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (std::is_same<T, __half>::value) asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <typename T> __device__ __forceinline__ uint32_t habsmax2_raw(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (std::is_same<T, __half>::value)
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 // ------------------------------------------------------------------------------------------
 // Varlen set-up: validate cu_seqlens and lay sequences out in 128-row aligned segments.
@@ -70,82 +109,134 @@ __global__ void __launch_bounds__(1024) varlen_setup_kernel(Problem p) {
 // K/V statistics of one block of tokens (KIND 0: K, the fixed-point sum, run only with
 // smooth_k; KIND 1: V, the fixed-point sum with smooth_v, and the min / max). Per (sequence,
 // kv head, channel). Grid: (token chunks, Hkv, batch). 256 threads: thread = (row group rg,
-// channel vector vec); TPR = padded head_dim / 8 threads per row.
+// channel vector vec); TPR = padded head_dim / 8 threads per row. A block walks nb <= 4
+// batches of 4 rows per thread (rows rg + RG * i), the next batch's loads in flight while the
+// current one is summed.
+//
+// Fixed-point sum, fast form (every |x| < 2^14 and, for bf16, no nonzero |x| < 2^-17, so that
+// x * 2^24 is an integer): hacc runs as 1.5 * 2^23 + sum(h), where h = round(16 x) is taken
+// against hacc itself (t = fl(hacc + 16 x), h = t - hacc, both exact in the binade
+// [2^23, 2^24) because a thread's at most 16 rows keep |sum h| <= 2^22), and racc sums the
+// exact remainders r = 16 x - h (|r| <= 1/2 on the 2^-20 lattice, |sum r| <= 8). Warps that
+// see any other value redo their rows with exact int64 conversions.
 template <typename T, int TPR, int KIND>
-__device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int hk, int b) {
+__device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int hk, int b, int nb) {
   constexpr int RG = 256 / TPR;
-  constexpr int kRows = 4;                 // rows per thread
-  constexpr int kChunk = kRows * RG;       // tokens per block: stats_chunk(8 * TPR)
+  constexpr bool kBf16 = !std::is_same<T, __half>::value;
   const Seq s = get_seq(p, b);
-  const int t0 = chunk * kChunk;
+  const int t0 = chunk * RG * 4 * nb;
   if (t0 >= s.len_k) return;
-  const int t1 = min(t0 + kChunk, s.len_k);
+  const int t1 = min(t0 + RG * 4 * nb, s.len_k);
   const int vec = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = vec * 8;
   const bool active = c0 < p.d;
   const bool want_sum = KIND == 0 || p.smooth_v;
-  const float lim = p.varlen ? __double2float_ru(__ddiv_rn(274877906944.0, (double)s.len_k))
-                             : p.range_limit;
   const T* base = KIND == 0
       ? static_cast<const T*>(p.k) + (int64_t)b * p.k_sb + (int64_t)hk * p.k_sh
       : static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)hk * p.v_sh;
   const int64_t sn = KIND == 0 ? p.k_sn : p.v_sn;
-  unsigned hi[8], lo[8];  // biased split words, summed modulo 2^32
-  int nrows = 0;           // rows summed by this thread
-  float amax = 0.f;        // max |x| of those rows (range check)
-  float mn[8], mx[8];
+  // packed 16-bit accumulators over raw input words (two channels each): V's min / max, K's
+  // max |x|, and (bf16) the smallest nonzero magnitude, kept as the signed 16-bit value
+  // (|x| bits | 0x8000) - 1 so that zero maps to the largest one
+  uint32_t mn[4], mx[4], ax[4], nz[4];
+  float hacc[8], racc[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    mn[j] = kBf16 ? 0x7F807F80u : 0x7C007C00u;  // +inf pairs
+    mx[j] = kBf16 ? 0xFF80FF80u : 0xFC00FC00u;  // -inf pairs
+    ax[j] = 0u;
+    nz[j] = 0x7FFF7FFFu;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    hi[i] = lo[i] = 0u;
-    mn[i] = __int_as_float(0x7f800000);
-    mx[i] = __int_as_float(0xff800000);
+    hacc[i] = kRoundMagic;
+    racc[i] = 0.f;
   }
-  bool exact = true;  // every value went through the exact int32 split
-  if (active) {
-    // every row of this thread is requested before any is used
-    uint4 raw[kRows];
+
+  auto load_batch = [&](int k, uint4 (&dst)[4]) {
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const int t = t0 + rg + RG * r;
-      raw[r] = t < t1 ? load8_raw<T>(base + (int64_t)(s.tok0_k + t) * sn, c0, p.d, p.vec16)
-                      : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + rg + RG * (4 * k + i);
+      dst[i] = (active && t < t1) ? load8_raw<T>(base + (int64_t)(s.tok0_k + t) * sn, c0, p.d, p.vec16)
+                                  : make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 cur[4], nxt[4] = {};
+  load_batch(0, cur);
+  for (int k = 0; k < nb; ++k) {
+    if (k + 1 < nb) load_batch(k + 1, nxt);
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      if (t0 + rg + RG * r >= t1) continue;
-      float x[8];
-      unpack8<T>(raw[r], x);
-      ++nrows;
+    for (int i = 0; i < 4; ++i) {
+      const bool live = t0 + rg + RG * (4 * k + i) < t1;
+      const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (want_sum) {
-          amax = fmaxf(amax, fabsf(x[i]));
-          exact &= fixed_split_exact<T>(x[i]);
-          unsigned h, l;
-          fixed_split_biased(x[i], h, l);
-          hi[i] += h;
-          lo[i] += l;
+      for (int j = 0; j < 4; ++j) {
+        if (KIND == 1 && live) {
+          mn[j] = hmin2_raw<T>(mn[j], w[j]);
+          mx[j] = hmax2_raw<T>(mx[j], w[j]);
         }
-        if (KIND == 1) {
-          mn[i] = fminf(mn[i], x[i]);
-          mx[i] = fmaxf(mx[i], x[i]);
+        if (want_sum) {
+          if (KIND == 0) ax[j] = habsmax2_raw<T>(ax[j], w[j]);
+          if (kBf16) nz[j] = min_s16x2(nz[j], (w[j] | 0x80008000u) - 0x00010001u);
+          float x0, x1, t0f, t1f, n0, n1, r0, r1;
+          unpack2<T>(w[j], x0, x1);
+          fma2(t0f, t1f, x0, x1, 16.0f, 16.0f, hacc[2 * j], hacc[2 * j + 1]);  // hacc + round(16 x)
+          fma2(n0, n1, t0f, t1f, -1.0f, -1.0f, hacc[2 * j], hacc[2 * j + 1]);  // -round(16 x)
+          fma2(r0, r1, x0, x1, 16.0f, 16.0f, n0, n1);                          // exact remainder
+          add2(racc[2 * j], racc[2 * j + 1], racc[2 * j], racc[2 * j + 1], r0, r1);
+          hacc[2 * j] = t0f;
+          hacc[2 * j + 1] = t1f;
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
   }
-  if (want_sum && amax >= lim) record_error(p.err, kDevRange);
+
+  // largest magnitude (range check and fast-form bound) and the bf16 small-value test
+  float amax = 0.f;
+  bool fast = true;
+  const bool seen = active && t0 + rg < t1;  // V: this thread's min / max hold a row
+  if (want_sum) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a0, a1, b0, b1;
+      if (KIND == 0) {
+        unpack2<T>(ax[j], a0, a1);
+        amax = fmaxf(amax, fmaxf(fabsf(a0), fabsf(a1)));
+      } else if (seen) {
+        unpack2<T>(mn[j], a0, a1);
+        unpack2<T>(mx[j], b0, b1);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
+      }
+      // a nonzero bf16 magnitude below 2^-17 (bits 1 .. 0x36FF) leaves a value below
+      // -32768 + 0x36FF in its half of nz
+      if (kBf16)
+        fast &= static_cast<int16_t>(nz[j] & 0xFFFFu) >= -32768 + 0x36FF &&
+                static_cast<int16_t>(nz[j] >> 16) >= -32768 + 0x36FF;
+    }
+    fast &= amax < 16384.0f;
+    const float lim = p.varlen ? __shfl_sync(0xffffffffu,
+                                             (threadIdx.x & 31) == 0
+                                                 ? __double2float_ru(__ddiv_rn(274877906944.0, (double)s.len_k))
+                                                 : 0.f,
+                                             0)
+                               : p.range_limit;
+    if (amax >= lim) record_error(p.err, kDevRange);
+  }
+  // sum(x * 2^24) = 2^20 sum(h) + 2^20 sum(r): |sum h| <= 2^22 sits in hacc's low mantissa
+  // bits, and 2^20 sum(r) (an integer, at most 2^23) converts exactly
   long long sum[8];
-  const unsigned bias = static_cast<unsigned>(nrows) * static_cast<unsigned>(kRoundMagicBits);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    sum[i] = (static_cast<long long>(static_cast<int>(hi[i] - bias)) << 20) +
-             static_cast<int>(lo[i] - bias);
-  if (!std::is_same<T, __half>::value && want_sum && !__all_sync(0xffffffffu, exact)) {
-    // a bf16 value below 2^-17 or above 2^18 in this warp: exact int64 conversion instead
+    sum[i] = (static_cast<long long>(static_cast<int>(__float_as_uint(hacc[i]) - kRoundMagicBits)) << 20) +
+             __float2int_rn(__fmul_rn(racc[i], 1048576.0f));
+  if (want_sum && !__all_sync(0xffffffffu, fast)) {
+    // exact int64 conversion of every row of this warp's threads instead
 #pragma unroll
     for (int i = 0; i < 8; ++i) sum[i] = 0;
     if (active) {
-      for (int r = 0; r < kRows; ++r) {
+      for (int r = 0; r < 4 * nb; ++r) {
         const int t = t0 + rg + RG * r;
         if (t >= t1) continue;
         float x[8];
@@ -155,6 +246,14 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
       }
     }
   }
+  float fmn[8], fmx[8];
+  if (KIND == 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      unpack2<T>(mn[j], fmn[2 * j], fmn[2 * j + 1]);
+      unpack2<T>(mx[j], fmx[2 * j], fmx[2 * j + 1]);
+    }
+  }
   // reduce the row groups that share a warp, then the 8 warps through shared memory
 #pragma unroll
   for (int off = TPR; off < 32; off <<= 1) {
@@ -162,8 +261,8 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
     for (int i = 0; i < 8; ++i) {
       if (want_sum) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], off);
       if (KIND == 1) {
-        mn[i] = fminf(mn[i], __shfl_xor_sync(0xffffffffu, mn[i], off));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
+        fmn[i] = fminf(fmn[i], __shfl_xor_sync(0xffffffffu, fmn[i], off));
+        fmx[i] = fmaxf(fmx[i], __shfl_xor_sync(0xffffffffu, fmx[i], off));
       }
     }
   }
@@ -188,7 +287,7 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
   if (KIND == 1) {
     if (lane < TPR) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = mn[i];
+      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = fmn[i];
     }
     __syncthreads();
     if (threadIdx.x < p.d) {
@@ -199,7 +298,7 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
     __syncthreads();
     if (lane < TPR) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = mx[i];
+      for (int i = 0; i < 8; ++i) red_f[warp][c0 + i] = fmx[i];
     }
     __syncthreads();
     if (threadIdx.x < p.d) {
@@ -211,14 +310,15 @@ __device__ __forceinline__ void kv_stats_block(const Problem& p, int chunk, int 
 }
 
 // Both tensors' statistics in one launch. Grid: (token chunks, Hkv, batch x tensors): blockIdx.z
-// = b + batch * t, t = 0 for K (present only with smooth_k) and the last t for V.
+// = b + batch * t, t = 0 for K (present only with smooth_k) and the last t for V; each chunk
+// is nb batches of 4 * RG tokens.
 template <typename T, int TPR>
-__global__ void __launch_bounds__(256, 4) kv_stats_kernel(Problem p) {
+__global__ void __launch_bounds__(256, 3) kv_stats_kernel(Problem p, int nb) {
   pdl_trigger();
   const int b = blockIdx.z % p.batch;
   const bool is_k = p.smooth_k && (int)blockIdx.z < p.batch;
-  if (is_k) kv_stats_block<T, TPR, 0>(p, blockIdx.x, blockIdx.y, b);
-  else kv_stats_block<T, TPR, 1>(p, blockIdx.x, blockIdx.y, b);
+  if (is_k) kv_stats_block<T, TPR, 0>(p, blockIdx.x, blockIdx.y, b, nb);
+  else kv_stats_block<T, TPR, 1>(p, blockIdx.x, blockIdx.y, b, nb);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -314,19 +414,37 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     base = static_cast<const T*>(p.v) + (int64_t)b * p.v_sb + (int64_t)h * p.v_sh; sn = p.v_sn;
   }
   const int tok0 = kIsQ ? s.tok0_q : s.tok0_k;
+  // tile row of the thread's i-th row: E4M3 V (kind 2) gives each thread RPT consecutive
+  // tokens, so that four of them form one 32-bit word of the transposed tile; the other kinds
+  // interleave the row groups
+  auto row_of = [&](int i) { return kind == 2 ? RPT * rg + i : rg + RG * i; };
   uint4 raw[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const int r = r0 + rg + RG * i;
+    const int r = r0 + row_of(i);
     raw[i] = (r < len && c0 < d) ? load8_raw<T>(base + (int64_t)(tok0 + r) * sn, c0, d, p.vec16)
                                  : make_uint4(0, 0, 0, 0);
   }
   // smoothed fp32 values of row i (x - mean, one IEEE subtraction; 0 past the end / past d)
   auto row_values = [&](int i, float (&x)[8]) {
     unpack8<T>(raw[i], x);
-    const bool live = r0 + rg + RG * i < len;
+    const bool live = r0 + row_of(i) < len;
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = (live && c0 + j < d) ? __fsub_rn(x[j], mean[j]) : 0.f;
+  };
+  // the same values in packed arithmetic (x + (-mean) is the same IEEE operation), without the
+  // row test: rows past the end read as 0 and give -mean here, and the kinds that use this
+  // form zero such rows' maxima and codes themselves; channels past d give 0 - 0
+  float nmean[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) nmean[j] = -mean[j];
+  auto row_fast = [&](int i, float (&x)[8]) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      unpack2<T>(w[j], x[2 * j], x[2 * j + 1]);
+      if (!kIsQ) add2(x[2 * j], x[2 * j + 1], x[2 * j], x[2 * j + 1], nmean[2 * j], nmean[2 * j + 1]);
+    }
   };
 
   if constexpr (kind == 3 || kind == 6) {
@@ -400,20 +518,33 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     return;
   }
   if constexpr (kind == 2) {
-    // ---- V: E4M3 codes, transposed through shared memory
+    // ---- V: E4M3 codes, transposed through shared memory. Four consecutive tokens of a
+    // channel form one 32-bit word; word w of channel row c sits in 16-byte chunk
+    // (w / 4) ^ ((c / 8) & 7), so the warp's stores spread over the banks.
     __shared__ __align__(16) uint8_t vtile[128][kTileRows];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int rr = rg + RG * i;
-      float x[8];
-      row_values(i, x);
+    for (int qd = 0; qd < RPT / 4; ++qd) {
+      uint32_t cw[4][4];  // [token][channel pair]: E4M3 bytes of channels 2j (low), 2j + 1
 #pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const uint32_t two = pack_e4m3x2(__fmul_rn(x[j], rcpv[j]), __fmul_rn(x[j + 1], rcpv[j + 1]));
-        if (c0 + j < dp) {
-          const int sw = (vec & 7) << 4;  // 16-byte chunk swizzle per channel octet
-          vtile[c0 + j][rr ^ sw] = static_cast<uint8_t>(two & 0xFF);
-          vtile[c0 + j + 1][rr ^ sw] = static_cast<uint8_t>(two >> 8);
+      for (int t = 0; t < 4; ++t) {
+        const int i = 4 * qd + t;
+        float x[8], y[8];
+        row_fast(i, x);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], x[j], x[j + 1], rcpv[j], rcpv[j + 1]);
+        const bool live = r0 + row_of(i) < len;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cw[t][j] = live ? pack_e4m3x2(y[2 * j], y[2 * j + 1]) : 0u;
+      }
+      const int tw = (RPT / 4) * rg + qd;                      // token word within the row
+      const int byte = (((tw >> 2) ^ (vec & 7)) << 4) + ((tw & 3) << 2);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (c0 + 2 * j < dp) {
+          const uint32_t lo01 = __byte_perm(cw[0][j], cw[1][j], 0x5410);  // t0c0 t0c1 t1c0 t1c1
+          const uint32_t lo23 = __byte_perm(cw[2][j], cw[3][j], 0x5410);  // t2c0 t2c1 t3c0 t3c1
+          *reinterpret_cast<uint32_t*>(&vtile[c0 + 2 * j][byte]) = __byte_perm(lo01, lo23, 0x6420);
+          *reinterpret_cast<uint32_t*>(&vtile[c0 + 2 * j + 1][byte]) = __byte_perm(lo01, lo23, 0x7531);
         }
       }
     }
@@ -440,13 +571,13 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     float x[8];
-    row_values(i, x);
+    row_fast(i, x);
     float a = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
 #pragma unroll
     for (int off = 1; off < TPR; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if (vec == 0) rowmax[rg + RG * i] = a;
+    if (vec == 0) rowmax[rg + RG * i] = r0 + rg + RG * i < len ? a : 0.f;  // past the end: 0
   }
   __syncthreads();
   const int64_t plane = plane_of(p, b, h, kIsQ ? p.hq : p.hkv);
@@ -490,7 +621,7 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     const int r = r0 + rr;
     const float rc = grcp[rr / gs];
     float x[8];
-    row_values(i, x);
+    row_fast(i, x);
     __align__(16) __half2 hv[4];
     if constexpr (kFp4) {
       // u = fl32(x * r); the 16-channel block of this row spans this thread and its
@@ -511,13 +642,19 @@ __device__ __forceinline__ void quant_block(const Problem& p, int tile, int h, i
     } else {
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        // rint_even(fl32(x * r)) via the rounding constant (|x * r| <= 127.00002 < 2^22)
-        float c0 = __fsub_rn(__fadd_rn(__fmul_rn(x[j], rc), kRoundMagic), kRoundMagic);
-        float c1 = __fsub_rn(__fadd_rn(__fmul_rn(x[j + 1], rc), kRoundMagic), kRoundMagic);
-        c0 = fminf(fmaxf(c0, -127.0f), 127.0f);
-        c1 = fminf(fmaxf(c1, -127.0f), 127.0f);
+        // rint_even(fl32(x * r)) via the rounding constant. Scalar IEEE operations on purpose:
+        // the compiler may fuse a packed multiply and the packed add after it into one packed
+        // fma, whose single rounding moves products that round to a tie (63.5) in fp32. No
+        // clamp is needed: r = fl32(127 / absmax) exceeds 127 / absmax by at most a relative
+        // 2^-24, so |fl32(x * r)| <= 127 + 2^-17 and its rounding is at most 127.
+        const float c0 = __fsub_rn(__fadd_rn(__fmul_rn(x[j], rc), kRoundMagic), kRoundMagic);
+        const float c1 = __fsub_rn(__fadd_rn(__fmul_rn(x[j + 1], rc), kRoundMagic), kRoundMagic);
         hv[j / 2] = __floats2half2_rn(c0, c1);  // exact: integers of magnitude <= 127
       }
+    }
+    if (r >= len) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) hv[j] = __half2{};  // rows past the end are stored as zeros
     }
     if (c0 < dp && r < stored)
       *reinterpret_cast<uint4*>(codes + (plane * rows_pp + row0 + r) * dp + c0) =
@@ -612,17 +749,24 @@ cudaError_t launch_varlen_setup(const Problem& p, cudaStream_t st) {
 }
 
 template <typename T>
-static void launch_kv_stats_t(const Problem& p, dim3 grid, cudaStream_t st) {
-  grid.z *= p.smooth_k ? 2 : 1;
-  if (p.dp == 64) kv_stats_kernel<T, 8><<<grid, 256, 0, st>>>(p);
-  else kv_stats_kernel<T, 16><<<grid, 256, 0, st>>>(p);
+static void launch_kv_stats_t(const Problem& p, dim3 grid, int nb, cudaStream_t st) {
+  if (p.dp == 64) kv_stats_kernel<T, 8><<<grid, 256, 0, st>>>(p, nb);
+  else kv_stats_kernel<T, 16><<<grid, 256, 0, st>>>(p, nb);
 }
 
 cudaError_t launch_kv_stats(const Problem& p, int max_len_k, cudaStream_t st) {
-  const int chunk = stats_chunk(p.dp);
-  const dim3 grid((max_len_k + chunk - 1) / chunk, p.hkv, p.batch);
-  if (p.dtype == 0) launch_kv_stats_t<__half>(p, grid, st);
-  else launch_kv_stats_t<__nv_bfloat16>(p, grid, st);
+  // tokens per batch (4 rows per thread); batches per block: 4 where that still leaves twelve
+  // blocks for each of the 152 SMs, else fewer
+  const int batch_rows = stats_chunk(p.dp);
+  const int tensors = p.smooth_k ? 2 : 1;
+  int nb = 4;
+  auto blocks = [&](int n) {
+    return (int64_t)((max_len_k + batch_rows * n - 1) / (batch_rows * n)) * p.hkv * p.batch * tensors;
+  };
+  while (nb > 1 && blocks(nb) < 152 * 12) nb >>= 1;
+  const dim3 grid((max_len_k + batch_rows * nb - 1) / (batch_rows * nb), p.hkv, p.batch * tensors);
+  if (p.dtype == 0) launch_kv_stats_t<__half>(p, grid, nb, st);
+  else launch_kv_stats_t<__nv_bfloat16>(p, grid, nb, st);
   return cudaGetLastError();
 }
 

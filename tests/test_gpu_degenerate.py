@@ -112,3 +112,31 @@ def test_inputs_at_the_fp16_extremes(path):
     k = (k.float() * 4e-5).half()
     assert (k.abs() < 6.1e-5).float().mean() > 0.5  # mostly subnormal
     _check(w, q, k, v, path=path)
+
+
+@pytest.mark.parametrize("heads,n", [(2, 1000), (128, 4096)], ids=["one_batch_per_block", "four_batches_per_block"])
+def test_bf16_means_beyond_the_packed_sum(heads, n):
+    # bf16 K and V with nonzero magnitudes below 2^-17 in some rows of some heads and
+    # magnitudes of 2^14 and more in others (a third of the heads stays ordinary): the
+    # statistics pass's packed fixed-point sum covers neither, so those warps redo their rows
+    # with exact int64 conversions; every smoothing mean stays bit-exact. The larger case
+    # gives each statistics block four batches of rows.
+    import quantized_attention_mean_gb300 as qa
+    from oracle.quant import fixed_point_mean
+    w = Workload("bf16_ranges", 1, heads, heads, 128, n, 64, dtype="bf16", gran="per_warp",
+                 accum="fp16+fp32", smooth_v=True)
+    q, k, v = dense_inputs(w, 5)
+    k, v = k.float(), v.float()
+    k[:, 0::3, 3::97, :] *= 2.0 ** -20          # |x| ~ 1e-6, below 2^-17 = 7.6e-6
+    v[:, 0::3, 11::83, :] *= 2.0 ** -21
+    k[:, 1::3, 5::89, 7] = 3.0e4                # above the packed sum's 2^14
+    v[:, 1::3, 17::101, 3] = -2.5e4
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    g = run_gpu_dense(w, q, k, v, path="main")
+    assert g["status"] == 0
+    ex = qa.export_quant(g["ws"], w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran)
+    km, vm = ex["kmean"].cpu().numpy(), ex["vmean"].cpu().numpy()
+    kn, vn = to_hnd_f32(k, w.layout), to_hnd_f32(v, w.layout)
+    for h in range(heads):
+        np.testing.assert_array_equal(km[0, h].view(np.uint32), fixed_point_mean(kn[0, h]).view(np.uint32))
+        np.testing.assert_array_equal(vm[0, h].view(np.uint32), fixed_point_mean(vn[0, h]).view(np.uint32))

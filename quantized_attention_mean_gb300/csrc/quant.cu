@@ -3,12 +3,14 @@
 // scales, and per-channel FP8 E4M3 quantisation of V.
 //
 // Both kernels are HBM-bound streaming passes: each block walks a tile of tokens with
-// 16-byte vector loads (8 channels per thread, 16 threads per token row), reduces with
-// warp shuffles and shared memory, and writes coalesced outputs.
+// 16-byte vector loads (8 channels per thread, head_dim / 8 threads per token row), reduces
+// with warp shuffles and shared memory, and writes coalesced outputs.
 //
 // Bit-exactness: the mean is an exact fixed-point sum (order-free, so atomics are fine);
-// scales and codes use explicitly rounded IEEE operations (__fdiv_rn, __fmul_rn, __fsub_rn,
-// __float2int_rn) so no contraction or reassociation can change a code.
+// scales and codes use explicitly rounded IEEE operations: scalar __fdiv_rn, __fmul_rn,
+// __fadd_rn / __fsub_rn, and packed f32x2 operations only where no multiply is followed by an
+// add (the compiler may fuse a packed multiply and add into one packed fma), so no
+// contraction or reassociation can change a code.
 #include "launch.h"
 #include "problem.cuh"
 #include "sm103_ptx.cuh"

@@ -266,9 +266,9 @@ __device__ __forceinline__ float max16(const float (&e)[16]) {
 // FP4 carriers of one 16-key group of y = 448 p values (y >= 0): the block scale is the
 // E4M3 rounding of the group's largest y, the codes e2m1(fl32(y . fl32(6 / scale))); rho_tab
 // holds fl32(6 / s) for every non-negative E4M3 code s.
-__device__ __forceinline__ void fp4_p_group(const float (&e)[16], const float* rho_tab,
+__device__ __forceinline__ void fp4_p_group(const float (&e)[16], float emax, const float* rho_tab,
                                             uint32_t (&w)[8]) {
-  const uint32_t code = pack_e4m3x2(max16(e), 0.f);
+  const uint32_t code = pack_e4m3x2(emax, 0.f);
   const __half2 s2 = e4m3x2_to_half2((code & 0xffu) * 0x101u);
   const float rho = rho_tab[code & 0x7fu];
 #pragma unroll
@@ -307,7 +307,7 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
           add2(a0, a1, a0, a1, e[u], e[u + 1]);
           add2(a0, a1, a0, a1, e[u + 2], e[u + 3]);
         }
-        fp4_p_group(e, rho_tab, w);
+        fp4_p_group(e, max16(e), rho_tab, w);
       } else {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -339,7 +339,8 @@ __device__ __noinline__ float masked_tile_exp(uint32_t tS, int limit, Mult8 cg, 
 template <int PV, int DP>
 __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const float (&cg)[8],
                                               float bias, uint8_t* my_p, int r,
-                                              const float* rho_tab, float (&gsum)[8]) {
+                                              const float* rho_tab, float (&gsum)[8],
+                                              const float (&gm)[8]) {
   constexpr bool PV16 = PV != 0, FP4 = PV == 2;
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
@@ -369,7 +370,12 @@ __device__ __forceinline__ void tile_exp_regs(const uint32_t (&sr)[4][32], const
         w[q4] = pack_p2<false>(e0, e1) | (pack_p2<false>(e2, e3) << 16);
       }
     }
-    if constexpr (FP4) fp4_p_group(eg, rho_tab, w);
+    if constexpr (FP4) {
+      // at head_dim 64 the group's largest value is the exponential of its largest score
+      // (c_g >= 0, and the fma and the exponential are monotone), one ex2 instead of a max
+      // over 16 values; at 128 the maxima come per 32 keys and the 16 values are compared
+      fp4_p_group(eg, DP == 64 ? ex2(fmaf(gm[g], cg[g], bias)) : max16(eg), rho_tab, w);
+    }
     if constexpr (!PV16 && DP == 64) {
       // (the same swizzled 16-byte unit as store_p_group, addressed in the shared window:
       // measured faster at head_dim 64)
@@ -429,7 +435,7 @@ __device__ __forceinline__ void tmem_wait_ld_max(float (&m)[8]) {
 // measured slower than the 32-column one).
 template <int DP>
 __device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32], const float (&cg)[8],
-                                              int lgk) {
+                                              int lgk, float (&gm)[8]) {
   if (DP == 128 && lgk == 6) {
     float cm[4];
     tmem_ld32_max(tS + 0, sr[0], cm[0]);
@@ -444,7 +450,6 @@ __device__ __forceinline__ float tile_max_regs(uint32_t tS, uint32_t (&sr)[4][32
     return fmaxf(fmaxf(cm[0] * cg[0], cm[1] * cg[2]), fmaxf(cm[2] * cg[4], cm[3] * cg[6]));
   }
   {
-    float gm[8];
     tmem_ld16_max<0>(tS + 0, sr[0], gm[0]);
     tmem_ld16_max<16>(tS + 16, sr[0], gm[1]);
     tmem_ld16_max<0>(tS + 32, sr[1], gm[2]);
@@ -860,6 +865,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int g = 0; g < 8; ++g) cg[g] = row_scale * skn[g];
         uint32_t sr[4][32];
+        float gmx[8];  // the scores' 16-key group maxima (unmasked tiles)
         float tile_max = __int_as_float(0xff800000);
         float m_new, alpha, bias;
         uint8_t* const my_p = p_row + (j % C::kPBufs) * C::kPTileBytes;
@@ -889,12 +895,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // 0.1278 ms)
         if constexpr (DP == 64) {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk);
+            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk, gmx);
             trace<TRACE>(p, trs, x, j, 1);
             trace<TRACE>(p, trs, x, j, 2);
             new_max();
             trace<TRACE>(p, trs, x, j, 4);
-            if (ok) tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum);
+            if (ok) tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum, gmx);
           } else {
             tile_max = masked_tile_max(tS, limit, c8);
             trace<TRACE>(p, trs, x, j, 1);
@@ -906,7 +912,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
         } else {
           if (__builtin_expect(!masked, 1)) {
-            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk);
+            tile_max = tile_max_regs<DP>(tS, sr, cg, lgk, gmx);
             tc_fence_before();
             mbar_arrive(&s_free[x]);
           } else {
@@ -918,7 +924,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
           trace<TRACE>(p, trs, x, j, 4);
           if (__builtin_expect(!masked, 1)) {
-            tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum);
+            tile_exp_regs<PV, DP>(sr, cg, bias, my_p, r, rho_tab, gsum, gmx);
           } else {
             gsum[0] = masked_tile_exp<PV>(tS, limit, c8, bias, my_p, r, rho_tab);
             tc_fence_before();

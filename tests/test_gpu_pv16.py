@@ -5,8 +5,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import (TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, cosine, gpu_kw, max_abs_excess,
-                     oracle_kw, out_to_hnd)
+from helpers import (TOL_COS, TOL_COS_FP64, TOL_LSE, TOL_MAX_ABS, assert_online_parity, cosine, gpu_kw,
+                     max_abs_excess, oracle_kw, out_to_hnd)
 from oracle.attention import attention_fp64, sage_attention
 from quantized_attention_mean_gb300.workloads import WORKLOADS, Workload, dense_inputs, to_hnd_f32
 
@@ -66,3 +66,23 @@ def test_pv16_more_accurate_than_fp8_on_the_gpu():
     sm = 1.0 / np.sqrt(128.0)
     exact = np.stack([attention_fp64(qn[0, h], kn[0, h], vn[0, h], sm, False)[0] for h in range(4)])
     assert np.abs(o16[0] - exact).max() < np.abs(o8[0] - exact).max()
+
+
+def test_pv16_full_size_sampled_rows():
+    # the DiT shape's head geometry (17776 keys, d = 64, 139 key tiles with the 112-row tail) on
+    # two heads; sampled query rows across the tiles, against the oracle's online form
+    import quantized_attention_mean_gb300 as qa
+    w = Workload("dit_pv16_h2", 1, 2, 2, 17776, 17776, 64, dtype="bf16", gran="per_warp",
+                 accum="fp16+fp32", smooth_v=True, k_offset_std=4.0, v_offset_std=2.0,
+                 return_lse=True)
+    q, k, v = dense_inputs(w, 4)
+    qn, kn, vn = (to_hnd_f32(t, w.layout) for t in (q, k, v))
+    dev = torch.device("cuda:0")
+    ws = qa.alloc_workspace(qa.workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.gran), dev)
+    out, lse = qa.sage_attn_qk_int8_pv_fp16(q.to(dev), k.to(dev), v.to(dev), workspace=ws, **gpu_kw(w))
+    torch.cuda.synchronize()
+    assert qa.read_device_status(ws) == 0
+    rows = np.array([0, 1, 127, 128, 4097, 9000, 17663, 17664, 17700, 17775])
+    ref = sage_attention(qn, kn, vn, pv="fp16", p_max="running", rows=rows, **oracle_kw(w))
+    o = out_to_hnd(out, w.layout)[:, :, rows]
+    assert_online_parity(o, ref["o"], w.dtype, lse.cpu().numpy()[:, :, rows], ref["lse"])

@@ -79,6 +79,10 @@ WORKLOADS = {
                              v_offset_std=2.0, extra={"pv": "fp4"}),
     "sdpa4k_fp4": Workload("sdpa4k_fp4", 2, 8, 8, 4096, 4096, 128, gran="per_warp",
                            accum="fp16+fp32", extra={"pv": "fp4"}),
+    # the FP4 variant on half the DiT heads at batch 1 (a profiling case, as dit17776_h24)
+    "dit17776_fp4_h24": Workload("dit17776_fp4_h24", 1, 24, 24, 17776, 17776, 64, dtype="bf16",
+                                 gran="per_warp", accum="fp16+fp32", smooth_v=True, k_offset_std=4.0,
+                                 v_offset_std=2.0, extra={"pv": "fp4"}),
     "varlen16": Workload("varlen16", 16, 32, 32, 0, 0, 128, gran="per_warp", accum="fp32",
                          varlen=True, n_seqs=16),
 }
